@@ -1,0 +1,398 @@
+#!/usr/bin/env python
+"""Benchmark of the chunkwise gated delta rule forward pass (libgdn).
+
+One step = one gdn_chunk_fwd over the training-shape workload
+(B4 H16 T4096 d_k=d_v=128, C64, bf16 q/k/v/o, fp32 gates and final state),
+inputs resident in HBM.  Prints one JSON line on rank 0.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+``--impl reference`` times the fp64 CPU oracle (the only other implementation
+of the method; there is no third-party one) on a bounded sample of the same
+workload on the host cores.  Under torchrun each rank runs its own replica of
+the workload (the method's (sequence, head) units are independent, so there is
+no collective on the data path); ``value`` is the tokens of all ranks over the
+slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "GDN chunk-fwd tokens/s and % bf16 tensor peak (B4 H16 T4096 d128)"
+WORKLOAD = "train_bf16"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_BYTES = 126 * 2 ** 20
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as fh:
+            d = json.load(fh)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def workload_numbers(w, lengths):
+    """Algorithmic FLOPs and bytes of one forward pass.
+
+    FLOPs: per chunk of n tokens and head, 2 [3 n d_k d_v + n^2 (3 d_k + 2 d_v)]
+    (K K^T, W, U, W S^T, Q S^T, Q K^T, P V_new, state update; C x C operands
+    counted dense).  Bytes: q, k, v read and o written once, 8 B of gates per
+    token-head, S0 read if given and S_final written, fp32.
+    """
+    esz = 2 if w.dtype == "bf16" else 4
+    flops = 0
+    for L in lengths:
+        full, tail = divmod(L, w.C)
+        for n in [w.C] * full + ([tail] if tail else []):
+            flops += 2 * (3 * n * w.dk * w.dv + n * n * (3 * w.dk + 2 * w.dv)) * w.H
+    tok_heads = sum(lengths) * w.H
+    nseq = len(lengths)
+    state = nseq * w.H * w.dv * w.dk * 4
+    byts = tok_heads * (2 * w.dk + 2 * w.dv) * esz + tok_heads * 8 + state
+    if w.s0 != "none":
+        byts += state
+    return flops, byts
+
+
+def kernel_source_sha():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "gated_delta_rule_09_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".h", ".cuh")):
+            with open(os.path.join(csrc, name), "rb") as fh:
+                h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the kernel sources as they are now (else None)."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    sha = kernel_source_sha()
+    for line in text.splitlines():
+        m = re.match(r"\s*(\w+)\s+sha=(\w+)\s+dram_bytes_per_launch=(\d+)", line)
+        if m and m.group(1) == workload and m.group(2) == sha:
+            return int(m.group(3))
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi sampled every 50 ms in the background."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.f = tempfile.TemporaryFile(mode="w+")
+        self.t0 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=timestamp," + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return []
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.seek(0)
+        rows = []
+        for line in self.f.read().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                ts += float("0." + parts[0].split(".")[1]) if "." in parts[0] else 0.0
+                rows.append(dict(ts=ts, sm=float(parts[2]), smax=float(parts[3]),
+                                 active=parts[5], hw=parts[6], hwt=parts[7], swt=parts[8],
+                                 pcap=parts[9]))
+            except (ValueError, IndexError):
+                continue
+        return rows
+
+    @staticmethod
+    def summarise(rows, t_start, t_end):
+        win = [r for r in rows if t_start - 0.1 <= r["ts"] <= t_end + 0.1]
+        if not win and rows:  # very short timed region: nearest samples
+            win = sorted(rows, key=lambda r: abs(r["ts"] - (t_start + t_end) / 2))[:3]
+        if not win:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        reasons = set()
+        for r in win:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                              ("swt", "sw_thermal_slowdown"), ("pcap", "sw_power_cap")):
+                if r[key].lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in win),
+                "sm_max_mhz": max(r["smax"] for r in win),
+                "reasons": sorted(reasons), "samples": len(win)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def cpu_baseline(w, x, sample_tokens):
+    """Oracle on one sequence x all heads x the first ``sample_tokens`` tokens."""
+    from oracle import gdn_recurrence_f64
+    sl = (slice(0, 1), slice(0, sample_tokens))
+    cores = os.cpu_count() or 1
+    args = [x[k][sl] for k in ("q", "k", "v", "log_alpha", "beta")]
+    t0 = time.perf_counter()
+    gdn_recurrence_f64(*args, n_threads=cores)
+    dt = time.perf_counter() - t0
+    return dict(value=sample_tokens / dt, unit="tokens/s", cores=min(cores, w.H), kind="oracle",
+                sample="1 of %d sequences x %d heads x first %d of %d tokens (%s), fp64, "
+                       "%.2f s" % (w.B, w.H, sample_tokens, w.T, w.name, dt))
+
+
+def run_reference(args, world, rank):
+    from gated_delta_rule_09_gb300 import inputs as I
+    if rank != 0:
+        return
+    w = I.WORKLOADS[args.workload]
+    x = I.generate(w, seed=0)
+    sample = args.ref_tokens
+    for _ in range(args.warmup):
+        cb = cpu_baseline(w, x, sample)
+    times = []
+    for _ in range(args.steps):
+        cb = cpu_baseline(w, x, sample)
+        times.append(sample / cb["value"])
+    total = sum(times)
+    value = args.steps * sample / total
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "%s: B%d H%d T%d d_k=%d d_v=%d C%d, each step a sample "
+                                   "of %d tokens x %d heads" % (w.name, w.B, w.H, w.T, w.dk,
+                                                                w.dv, w.C, sample, w.H)},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cb["cores"],
+                             "kind": "oracle", "sample": cb["sample"]},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, world, rank, local):
+    import torch
+    import gated_delta_rule_09_gb300 as gdn
+    from gated_delta_rule_09_gb300 import inputs as I
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = I.WORKLOADS[args.workload]
+    x = I.generate(w, seed=rank)
+    lengths = x["lengths"]
+    flops, byts = workload_numbers(w, lengths)
+    tokens = sum(lengths)
+    keys = ("q", "k", "v", "log_alpha", "beta")
+    # two resident copies, used alternately, so no step finds its inputs in L2
+    sets = []
+    for _ in range(2):
+        d = {kk: x[kk].to(dev) for kk in keys}
+        d["S0"] = None if x["S0"] is None else x["S0"].to(dev)
+        d["cu"] = None if x["cu_seqlens"] is None else x["cu_seqlens"].to(dev)
+        d["o"] = torch.empty(x["v"].shape, dtype=x["v"].dtype, device=dev)
+        d["Sf"] = torch.empty((x["N"], w.H, w.dv, w.dk), dtype=torch.float32, device=dev)
+        sets.append(d)
+    stream = torch.cuda.Stream(dev)
+
+    def step(i):
+        d = sets[i & 1]
+        gdn.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], S0=d["S0"],
+                          o=d["o"], S_final=d["Sf"], C=w.C, cu_seqlens=d["cu"], stream=stream)
+
+    with torch.cuda.stream(stream):
+        for i in range(max(args.warmup, 3)):
+            step(i)
+    torch.cuda.synchronize(dev)
+    assert gdn.gdn_get_device_status(stream) == 0
+    launches_per_step, path = gdn.gdn_last_launch_count()
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    t_start = time.time()
+    ev0.record(stream)
+    for i in range(args.steps):
+        step(i)
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    t_end = time.time()
+    barrier(world)
+    rows = sampler.stop()
+    ms = ev0.elapsed_time(ev1) / args.steps
+    ms_max = max_over_ranks(ms, world)
+    clocks = ClockSampler.summarise(rows, t_start, t_end)
+
+    # end to end through the public call: pinned host inputs -> device, the
+    # forward pass, and the result back to pinned host memory, every step
+    host = {kk: x[kk].pin_memory() for kk in keys}
+    host_S0 = None if x["S0"] is None else x["S0"].pin_memory()
+    host_cu = None if x["cu_seqlens"] is None else x["cu_seqlens"].pin_memory()
+    out_o = torch.empty(x["v"].shape, dtype=x["v"].dtype).pin_memory()
+    out_S = torch.empty((x["N"], w.H, w.dv, w.dk), dtype=torch.float32).pin_memory()
+    d = sets[0]
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    h2d += 0 if host_S0 is None else host_S0.numel() * 4
+    h2d += 0 if host_cu is None else host_cu.numel() * 4
+    d2h = out_o.numel() * out_o.element_size() + out_S.numel() * 4
+    e2e_steps = max(1, min(args.steps, args.e2e_steps))
+
+    def e2e_step():
+        for kk in keys:
+            d[kk].copy_(host[kk], non_blocking=True)
+        if host_S0 is not None:
+            d["S0"].copy_(host_S0, non_blocking=True)
+        if host_cu is not None:
+            d["cu"].copy_(host_cu, non_blocking=True)
+        gdn.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], S0=d["S0"],
+                          o=d["o"], S_final=d["Sf"], C=w.C, cu_seqlens=d["cu"], stream=stream)
+        out_o.copy_(d["o"], non_blocking=True)
+        out_S.copy_(d["Sf"], non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world)
+    barrier(world)
+
+    if rank != 0:
+        return
+    peaks, peak_src = load_peaks()
+    kernel_s = ms * 1e-3 / max(launches_per_step, 1)  # one launch per step on both paths
+    gbs = byts / kernel_s / 1e9
+    tflops = flops / (ms * 1e-3) / 1e12
+    value = world * tokens / (ms_max * 1e-3)
+    cb = (cpu_baseline(w, x, min(args.cpu_tokens, w.T or tokens))
+          if (world == 1 and not args.no_cpu_baseline) else None)
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": "%s: B%d H%d T%d d_k=%d d_v=%d C%d, bf16 q/k/v/o, fp32 gates "
+                               "and final state, no S0" % (w.name, w.B, w.H, w.T, w.dk, w.dv, w.C),
+                   "tokens_per_step": tokens, "l2": "inputs larger than L2 (%.0f MB moved per "
+                   "step vs %.0f MB L2), two resident input copies used alternately"
+                   % (byts / 1e6, L2_BYTES / 1e6),
+                   "parallelism": "replicas x%d" % world,
+                   "kernel_path": "tcgen05" if path == 1 else "fp32 cuda-core"},
+        "tflops": tflops,
+        "pct_bf16_peak": 100.0 * tflops / peaks["bf16_tflops"],
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": gbs / peaks["hbm_gbs"], "traffic": recorded_traffic(w.name),
+                     "algorithmic_bytes": byts, "peak_source": peak_src,
+                     "tensor": {"achieved": tflops, "peak": peaks["bf16_tflops"],
+                                "unit": "TFLOP/s", "frac": tflops / peaks["bf16_tflops"],
+                                "algorithmic_flops": flops}},
+        "clocks": clocks,
+        "e2e": {"value": world * tokens / (e2e_ms * 1e-3), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": launches_per_step * args.steps,
+        "cpu_baseline": cb,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--ref-tokens", type=int, default=512,
+                    help="tokens per oracle sample (one sequence, all heads)")
+    ap.add_argument("--cpu-tokens", type=int, default=4096,
+                    help="tokens of the oracle sample for the cpu_baseline key")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_ours(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,107 @@
+"""GB300-native chunkwise forward pass of the gated delta rule.
+
+The compute runs in libgdn.so (hand-written CUDA for sm_103a) behind the C ABI
+of ``include/gdn.h``; this module only marshals torch CUDA tensors into that
+call.  Importing it loads the library and raises if it is missing.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import _lib
+from ._lib import GdnError, GDN_BF16, GDN_F32  # noqa: F401
+
+_DTYPES = {torch.float32: _lib.GDN_F32, torch.bfloat16: _lib.GDN_BF16}
+
+_lib.load()
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _need_cuda(name, t, dtype=None):
+    if t is None:
+        return
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError("%s must be a CUDA tensor" % name)
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+
+
+def gdn_chunk_fwd(q, k, v, log_alpha, beta, S0=None, o=None, S_final=None,
+                  C=64, cu_seqlens=None, stream=None, want_final_state=True):
+    """Chunkwise gated delta rule forward; returns ``(o, S_final)``.
+
+    q, k [B,T,H,d_k] and v [B,T,H,d_v] (fp32 or bf16, one dtype);
+    log_alpha, beta [B,T,H] fp32; S0 [N,H,d_v,d_k] fp32 or None.  With
+    ``cu_seqlens`` (int32 CUDA tensor [N+1]) the inputs are packed with B == 1.
+    ``o`` / ``S_final`` may be passed preallocated; otherwise they are
+    allocated here.  Runs on ``stream`` (a torch.cuda.Stream, a raw handle, or
+    None for the current torch stream).
+    """
+    if q.dtype not in _DTYPES:
+        raise TypeError("q/k/v dtype must be float32 or bfloat16, got %s" % q.dtype)
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _need_cuda(name, t, q.dtype)
+    _need_cuda("log_alpha", log_alpha, torch.float32)
+    _need_cuda("beta", beta, torch.float32)
+    _need_cuda("S0", S0, torch.float32)
+    _need_cuda("cu_seqlens", cu_seqlens, torch.int32)
+    if q.dim() != 4 or k.shape != q.shape or v.dim() != 4 or v.shape[:3] != q.shape[:3]:
+        raise ValueError("q, k must be [B,T,H,d_k] and v [B,T,H,d_v]")
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    if log_alpha.shape != (B, T, H) or beta.shape != (B, T, H):
+        raise ValueError("log_alpha and beta must be [B,T,H]")
+    if cu_seqlens is not None:
+        if B != 1:
+            raise ValueError("packed (cu_seqlens) inputs must have B == 1")
+        N = cu_seqlens.numel() - 1
+    else:
+        N = B
+    if S0 is not None and S0.shape != (N, H, dv, dk):
+        raise ValueError("S0 must be [N,H,d_v,d_k] = %s" % ((N, H, dv, dk),))
+    if o is None:
+        o = torch.empty((B, T, H, dv), dtype=q.dtype, device=q.device)
+    _need_cuda("o", o, q.dtype)
+    if S_final is None and want_final_state:
+        S_final = torch.empty((N, H, dv, dk), dtype=torch.float32, device=q.device)
+    _need_cuda("S_final", S_final, torch.float32)
+    if stream is None:
+        handle = torch.cuda.current_stream(q.device).cuda_stream
+    elif isinstance(stream, torch.cuda.Stream):
+        handle = stream.cuda_stream
+    else:
+        handle = int(stream)
+    with torch.cuda.device(q.device):
+        st = _lib.load().gdn_chunk_fwd(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(S0),
+            _ptr(o), _ptr(S_final), N, H, T, dk, dv, int(C), _ptr(cu_seqlens),
+            _DTYPES[q.dtype], ctypes.c_void_p(handle))
+    _lib.check(st)
+    return o, S_final
+
+
+def gdn_get_device_status(stream=None):
+    """Synchronise and return (then clear) the device status bits."""
+    handle = (torch.cuda.current_stream().cuda_stream if stream is None
+              else getattr(stream, "cuda_stream", stream))
+    flags = ctypes.c_uint(0)
+    _lib.check(_lib.load().gdn_get_device_status(ctypes.c_void_p(handle), ctypes.byref(flags)))
+    return flags.value
+
+
+def gdn_last_launch_count():
+    """(kernels enqueued by the last gdn_chunk_fwd on this thread, path id)."""
+    path = ctypes.c_int(-1)
+    n = _lib.load().gdn_last_launch_count(ctypes.byref(path))
+    return n, path.value
+
+
+def gdn_version():
+    return _lib.load().gdn_version()

@@ -1,0 +1,26 @@
+// Internal interface between the C-ABI front end (gdn_api.cu) and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+struct GdnArgs {
+    const void *q, *k, *v;       // [*, T, H, dk] / [*, T, H, dv], dtype
+    const float *log_alpha;      // [*, T, H]
+    const float *beta;           // [*, T, H]
+    const float *S0;             // [N, H, dv, dk] or null
+    void *o;                     // [*, T, H, dv], dtype
+    float *S_final;              // [N, H, dv, dk] or null
+    int N, H, T, dk, dv, C;
+    const int32_t *cu_seqlens;   // device [N + 1] or null
+    int dtype;                   // 0 = fp32, 1 = bf16
+    unsigned int *status;        // device status word (GDN_DEV_* bits)
+};
+
+// fp32 CUDA-core kernel: every supported shape and dtype.
+cudaError_t gdn_launch_simt(const GdnArgs &a, cudaStream_t s, int *launches);
+size_t gdn_simt_smem_bytes(int C, int dk);
+
+// tcgen05 tensor-core kernel: bf16, the shapes gdn_tc_supported() accepts.
+bool gdn_tc_supported(const GdnArgs &a);
+cudaError_t gdn_launch_tc(const GdnArgs &a, cudaStream_t s, int *launches);

@@ -1,0 +1,135 @@
+/*
+ * gdn.h — C ABI of libgdn: the chunkwise-parallel forward pass of the gated
+ * delta rule on one NVIDIA GB300 (sm_103a).
+ *
+ * The operation (north-star recurrence; "从零开始的 GDN 推导", §"Gated Delta
+ * Rule Chunk-wise Parallel 前向推导", recurrent form, written here with column
+ * vectors so that the state S is d_v x d_k):
+ *
+ *     S_t = alpha_t * S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T
+ *     o_t = S_t q_t
+ *
+ * evaluated chunk by chunk with the WY / UT-transform form of the same page
+ * (§"UT transform", §"S 的推导", §"O 的推导", §"总结"): inside a chunk of C
+ * tokens everything is dense matrix algebra; only the d_v x d_k state is
+ * carried from one chunk to the next ("RNN的复兴03：现代RNN的并行计算", §四:
+ * parallel inside a chunk, dependent between chunks).  The result equals the
+ * sequential recurrence up to floating-point rounding.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Tensor pointers are DEVICE pointers (cudaMalloc / torch CUDA memory) on
+ *    the current device, row-major and contiguous.  The caller allocates and
+ *    owns all of them; the library keeps no reference after the call returns.
+ *  - The library allocates no device memory in these calls.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *    default stream): they validate on the host, enqueue kernels and return.
+ *  - On any status other than GDN_OK nothing was enqueued, and
+ *    gdn_get_last_error() returns a message for the calling thread.
+ *  - There is no CPU fallback: a call either runs its CUDA kernels or fails.
+ */
+#ifndef GDN_H_
+#define GDN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    GDN_OK = 0,
+    GDN_ERR_INVALID_ARG = 1, /* null/misaligned pointer, bad size, overlap   */
+    GDN_ERR_UNSUPPORTED = 2, /* shape or dtype outside the compiled set      */
+    GDN_ERR_CUDA = 3,        /* a CUDA runtime call or a launch failed        */
+    GDN_ERR_TIMEOUT = 4,     /* reserved: a bounded device wait ran out       */
+    GDN_ERR_INTERNAL = 5     /* reserved: inconsistent internal state         */
+} gdn_status_t;
+
+typedef enum { GDN_F32 = 0, GDN_BF16 = 1 } gdn_dtype_t;
+
+/* Device-side status bits returned by gdn_get_device_status(). */
+#define GDN_DEV_BAD_SEQLENS 0x1u /* a cu_seqlens span was negative or past T */
+#define GDN_DEV_WAIT_TIMEOUT 0x2u /* a bounded pipeline wait gave up          */
+
+/*
+ * gdn_chunk_fwd — forward pass of the gated delta rule, chunkwise.
+ *
+ * Arguments (N = B, the number of sequences):
+ *   q          [B, T, H, d_k]  dtype   queries
+ *   k          [B, T, H, d_k]  dtype   keys (the method assumes nothing about
+ *                                      their norm; unit norm is the usual input)
+ *   v          [B, T, H, d_v]  dtype   values
+ *   log_alpha  [B, T, H]       fp32    log of the decay gate alpha_t (<= 0 is
+ *                                      the usual range; not required)
+ *   beta       [B, T, H]       fp32    write strength beta_t (any real value;
+ *                                      (0, 2) is the extended DeltaNet range)
+ *   S0         [N, H, d_v, d_k] fp32   initial state per (sequence, head), or
+ *                                      NULL for zeros
+ *   o          [B, T, H, d_v]  dtype   output, o_t = S_t q_t (state after
+ *                                      token t); must not overlap any input
+ *   S_final    [N, H, d_v, d_k] fp32   state after each sequence's last token,
+ *                                      or NULL if not wanted; may be exactly
+ *                                      S0 (in-place carry), must not overlap
+ *                                      anything else
+ *   B, H, T    batch, heads, tokens per sequence
+ *   d_k, d_v   key and value head dimensions
+ *   C          chunk length: 16, 32 or 64
+ *   cu_seqlens device int32 [N + 1] or NULL.  When given, the sequences are
+ *              packed along the token axis: q/k/v/o are [1, T, H, *],
+ *              log_alpha/beta are [1, T, H], B is the number of sequences N,
+ *              sequence n spans tokens [cu_seqlens[n], cu_seqlens[n+1]), and
+ *              T is the packed length.  Chunks never cross a sequence; each
+ *              sequence starts from its own S0[n].  Spans that are negative or
+ *              run past T are skipped on the device and raise
+ *              GDN_DEV_BAD_SEQLENS (see gdn_get_device_status).
+ *   dtype      GDN_F32 or GDN_BF16 (q, k, v and o share it; the arithmetic is
+ *              fp32 in either case, with bf16 tensor-core operands for bf16)
+ *   stream     cudaStream_t to enqueue on
+ *
+ * Alignment: q, k, v, o must be aligned to 16 bytes; log_alpha, beta, S0 and
+ * S_final to 4 bytes (16 bytes lets the fastest path run).
+ * Supported shapes: d_k in [1, 128], d_v >= 1, C in {16, 32, 64}.  The
+ * tcgen05 tensor-core kernel serves the shapes listed at gdn_last_launch_count;
+ * every other supported shape runs on the fp32 CUDA-core kernel.  Both are
+ * CUDA kernels of this library.
+ *
+ * Returns GDN_OK once the work is enqueued, or an error status (nothing
+ * enqueued).  Errors detected by the kernels are reported through
+ * gdn_get_device_status().
+ */
+gdn_status_t gdn_chunk_fwd(const void *q, const void *k, const void *v,
+                           const float *log_alpha, const float *beta,
+                           const float *S0, void *o, float *S_final,
+                           int B, int H, int T, int d_k, int d_v, int C,
+                           const int32_t *cu_seqlens, gdn_dtype_t dtype,
+                           void *stream);
+
+/*
+ * gdn_get_device_status — synchronise `stream`, then read and clear the
+ * device-side status bits (GDN_DEV_*) raised by kernels of this library on the
+ * current device since the last read.  *flags receives the bits (0 = clean).
+ * Returns GDN_ERR_CUDA if synchronising or reading fails.
+ */
+gdn_status_t gdn_get_device_status(void *stream, unsigned int *flags);
+
+/* Message for the last non-OK status returned on the calling thread. */
+const char *gdn_get_last_error(void);
+
+/* Library version as MAJOR * 10000 + MINOR * 100 + PATCH. */
+int gdn_version(void);
+
+/*
+ * gdn_last_launch_count — number of kernels the last successful gdn_chunk_fwd
+ * on the calling thread enqueued, and in *path which kernel family ran
+ * (0 = fp32 CUDA-core kernel, 1 = tcgen05 tensor-core kernel).  For
+ * accounting in benchmarks; no device work.
+ */
+int gdn_last_launch_count(int *path);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_H_ */

@@ -1,0 +1,177 @@
+"""GPU parity: libgdn (through its C ABI) against the fp64 oracle.
+
+Tolerances (from the stated bar): fp32 inputs, relative L2 error <= 1e-4;
+bf16 inputs, max |x - ref| / RMS(ref) <= 2e-2, each applied separately to the
+output o and the final state S_final.
+"""
+import numpy as np
+import pytest
+import torch
+
+from gated_delta_rule_09_gb300 import inputs as I
+from oracle import gdn_recurrence_f64
+
+pytestmark = pytest.mark.gpu
+
+TOL_F32 = 1e-4
+TOL_BF16 = 2e-2
+
+
+@pytest.fixture(scope="module")
+def gdn():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import gated_delta_rule_09_gb300 as g
+    return g
+
+
+def _dev(x):
+    return {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
+
+
+def err(x, ref, dtype):
+    x = np.asarray(x, np.float64)
+    if dtype == "f32":
+        return float(np.linalg.norm(x - ref) / max(np.linalg.norm(ref), 1e-300))
+    return float(np.max(np.abs(x - ref)) / max(np.sqrt(np.mean(ref ** 2)), 1e-300))
+
+
+def run_and_check(gdn, x, C, dtype, S0=None, want_S=True, tol=None):
+    d = _dev(x)
+    S0_dev = d["S0"] if S0 is None else S0
+    o, S = gdn.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"],
+                             S0=S0_dev, C=C, cu_seqlens=d["cu_seqlens"],
+                             want_final_state=want_S)
+    assert gdn.gdn_get_device_status() == 0
+    ro, rS = gdn_recurrence_f64(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"],
+                                S0=x["S0"], cu_seqlens=x["cu_seqlens"])
+    tol = tol or (TOL_F32 if dtype == "f32" else TOL_BF16)
+    eo = err(o.double().cpu().numpy(), ro, dtype)
+    assert np.isfinite(eo) and eo <= tol, ("o", eo)
+    if want_S:
+        es = err(S.double().cpu().numpy(), rS, dtype)
+        assert np.isfinite(es) and es <= tol, ("S_final", es)
+    return o, S
+
+
+@pytest.mark.parametrize("name", list(I.WORKLOADS))
+def test_workload_full_size(gdn, name):
+    """Every named workload at its full size, all outputs compared."""
+    w = I.WORKLOADS[name]
+    x = I.generate(w, seed=0)
+    run_and_check(gdn, x, w.C, w.dtype)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("T,C", [(1, 16), (15, 16), (64, 16), (100, 32), (200, 64), (63, 64), (65, 64)])
+def test_ragged_lengths(gdn, dtype, T, C):
+    x = I.custom(2, 3, T, 32, 48, C, dtype=dtype, seed=T + C, s0="normal_0.02")
+    run_and_check(gdn, x, C, dtype)
+
+
+@pytest.mark.parametrize("dk,dv", [(16, 16), (64, 64), (128, 128), (64, 128), (128, 64),
+                                   (128, 256), (96, 192), (40, 24)])
+def test_head_dims(gdn, dk, dv):
+    x = I.custom(1, 2, 300, dk, dv, 64, dtype="bf16", seed=dk * 1000 + dv, s0="normal_0.02")
+    run_and_check(gdn, x, 64, "bf16")
+
+
+def test_varlen_edge_lengths(gdn):
+    """Packed sequences with empty, length-1, sub-chunk and ragged lengths."""
+    lens = [0, 1, 63, 64, 65, 130, 0, 7]
+    x = I.custom(1, 4, 0, 128, 128, 64, dtype="bf16", seed=5, lengths=lens, s0="normal_0.02")
+    run_and_check(gdn, x, 64, "bf16")
+
+
+def test_extended_beta_range(gdn):
+    """beta in (0, 2): the extended DeltaNet range (negative eigenvalues)."""
+    x = I.custom(2, 2, 256, 64, 64, 64, dtype="bf16", seed=3)
+    x["beta"] = x["beta"] * 2.0
+    run_and_check(gdn, x, 64, "bf16")
+
+
+def test_s0_none_equals_zeros_and_no_final_state(gdn):
+    x = I.custom(1, 2, 130, 64, 64, 64, dtype="bf16", seed=4)
+    d = _dev(x)
+    o1, S1 = gdn.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], C=64)
+    z = torch.zeros_like(S1)
+    o2, S2 = gdn.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], S0=z, C=64)
+    o3, S3 = gdn.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], C=64,
+                               want_final_state=False)
+    assert S3 is None
+    assert torch.equal(o1, o2) and torch.equal(S1, S2) and torch.equal(o1, o3)
+
+
+def test_in_place_state_and_resume(gdn):
+    """S_final == S0 in place, and (T1) then (T2, S0 = S_final) equals (T1 + T2)."""
+    x = I.custom(2, 2, 256, 64, 64, 64, dtype="bf16", seed=6, s0="normal_0.02")
+    d = _dev(x)
+    o_full, S_full = gdn.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"],
+                                       S0=d["S0"], C=64)
+    S = d["S0"].clone()
+    cut = 128  # a chunk boundary, so the chunk grid is the same in both runs
+    sl1 = lambda t: t[:, :cut].contiguous()
+    sl2 = lambda t: t[:, cut:].contiguous()
+    oa, _ = gdn.gdn_chunk_fwd(sl1(d["q"]), sl1(d["k"]), sl1(d["v"]), sl1(d["log_alpha"]),
+                              sl1(d["beta"]), S0=S, S_final=S, C=64)
+    ob, _ = gdn.gdn_chunk_fwd(sl2(d["q"]), sl2(d["k"]), sl2(d["v"]), sl2(d["log_alpha"]),
+                              sl2(d["beta"]), S0=S, S_final=S, C=64)
+    torch.cuda.synchronize()
+    assert torch.equal(torch.cat([oa, ob], 1), o_full)
+    assert torch.equal(S, S_full)
+
+
+def test_deterministic(gdn):
+    x = I.custom(2, 4, 500, 128, 128, 64, dtype="bf16", seed=7)
+    d = _dev(x)
+    a = gdn.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], C=64)
+    b = gdn.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], C=64)
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+def test_guard_bands_untouched(gdn):
+    """Writes stay inside o and S_final: canaries around both are unchanged."""
+    x = I.custom(1, 3, 200, 64, 96, 64, dtype="bf16", seed=8)
+    d = _dev(x)
+    B, T, H, _ = d["q"].shape
+    dv, dk = 96, 64
+    pad = 4096
+    ob = torch.full((2 * pad + B * T * H * dv,), float("nan"), dtype=torch.bfloat16, device="cuda")
+    sb = torch.full((2 * pad + H * dv * dk,), -7.0, dtype=torch.float32, device="cuda")
+    o = ob[pad:pad + B * T * H * dv].view(B, T, H, dv)
+    S = sb[pad:pad + H * dv * dk].view(1, H, dv, dk)
+    gdn.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], o=o, S_final=S, C=64)
+    torch.cuda.synchronize()
+    assert torch.isnan(ob[:pad].float()).all() and torch.isnan(ob[-pad:].float()).all()
+    assert (sb[:pad] == -7.0).all() and (sb[-pad:] == -7.0).all()
+    assert torch.isfinite(o.float()).all()
+
+
+def test_bad_cu_seqlens_sets_device_status(gdn):
+    """Malformed spans are skipped on the device and reported, not faulted."""
+    x = I.custom(1, 2, 0, 32, 32, 16, dtype="bf16", seed=9, lengths=[10, 10])
+    d = _dev(x)
+    bad = torch.tensor([0, 15, 5], dtype=torch.int32, device="cuda")   # decreasing span
+    gdn.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], C=16, cu_seqlens=bad)
+    assert gdn.gdn_get_device_status() & 0x1
+    past = torch.tensor([0, 10, 25], dtype=torch.int32, device="cuda")  # runs past T = 20
+    gdn.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], C=16, cu_seqlens=past)
+    assert gdn.gdn_get_device_status() & 0x1
+    assert gdn.gdn_get_device_status() == 0  # cleared by the read
+
+
+def test_sampled_outputs_at_full_size_train_shape(gdn):
+    """The benchmark's launch (B4 H16 T4096 d128, C64, bf16): outputs of a few
+    (sequence, head) units recomputed one by one by the oracle."""
+    w = I.WORKLOADS["train_bf16"]
+    x = I.generate(w, seed=1)
+    d = _dev(x)
+    o, S = gdn.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], C=64)
+    o = o.double().cpu().numpy()
+    S = S.double().cpu().numpy()
+    for b, h in ((0, 0), (3, 15), (1, 7)):
+        sl = (slice(b, b + 1), slice(None), slice(h, h + 1))
+        ro, rS = gdn_recurrence_f64(x["q"][sl], x["k"][sl], x["v"][sl],
+                                    x["log_alpha"][sl], x["beta"][sl])
+        assert err(o[sl], ro, "bf16") <= TOL_BF16
+        assert err(S[b:b + 1, h:h + 1], rS, "bf16") <= TOL_BF16

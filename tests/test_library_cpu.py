@@ -1,0 +1,92 @@
+"""The C-ABI library builds, loads, exports every symbol include/gdn.h declares,
+and rejects bad arguments on the host before touching the GPU (CPU only)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gdn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from gated_delta_rule_09_gb300 import build, _lib
+    build.build()
+    return _lib.load()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(gdn_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_header_declares_entry_points():
+    names = declared_functions()
+    for n in ("gdn_chunk_fwd", "gdn_get_last_error", "gdn_get_device_status",
+              "gdn_version", "gdn_last_launch_count"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    from gated_delta_rule_09_gb300 import _lib
+    out = subprocess.run(["nm", "-D", "--defined-only", _lib.LIB_PATH],
+                         capture_output=True, text=True, check=True).stdout
+    exported = set(l.split()[-1] for l in out.splitlines() if l.strip())
+    for name in declared_functions():
+        assert name in exported, name
+        assert hasattr(lib, name)
+    assert set(declared_functions()) == set(_lib.SIGNATURES)
+
+
+def test_header_compiles_as_c():
+    # The header is plain C: it must compile without CUDA headers.
+    src = '#include "gdn.h"\nint main(void){ return (int)GDN_OK + (int)GDN_BF16; }\n'
+    p = subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-I", os.path.dirname(HEADER),
+                        "-x", "c", "-", "-o", os.devnull], input=src, text=True,
+                       capture_output=True)
+    assert p.returncode == 0, p.stderr
+
+
+def _call(lib, q=0x1000, k=0x100000, v=0x200000, la=0x300000, be=0x400000, S0=None,
+          o=0x500000, Sf=None, B=1, H=1, T=16, dk=16, dv=16, C=16, cu=None, dtype=1):
+    return lib.gdn_chunk_fwd(q, k, v, la, be, S0, o, Sf, B, H, T, dk, dv, C, cu, dtype, None)
+
+
+def test_version(lib):
+    assert lib.gdn_version() == 100
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(C=48), 2), (dict(C=128), 2), (dict(dtype=7), 2), (dict(dk=129), 2),
+    (dict(B=-1), 1), (dict(T=-5), 1), (dict(dk=0), 1), (dict(dv=0), 1),
+    (dict(q=None), 1), (dict(o=None), 1), (dict(la=None), 1),
+    (dict(q=0x1002), 1), (dict(o=0x500008), 1), (dict(la=0x300002), 1),
+    (dict(o=0x1000), 1),                       # o aliases q
+    (dict(Sf=0x100000), 1),                    # S_final overlaps k
+    (dict(S0=0x600000, Sf=0x600040), 1),       # partial overlap of S0 / S_final
+    (dict(cu=0x700000, B=0), 1),
+])
+def test_host_validation(lib, kw, code):
+    st = _call(lib, **kw)
+    assert st == code, (kw, st, lib.gdn_get_last_error())
+    assert lib.gdn_get_last_error()  # a message is set
+
+
+def test_empty_problem_is_a_no_op(lib):
+    # No units: returns OK without any CUDA call (this host has no GPU).
+    assert _call(lib, B=0) == 0
+    assert _call(lib, H=0) == 0
+    n = ctypes.c_int(5)
+    assert lib.gdn_last_launch_count(ctypes.byref(n)) == 0
+
+
+def test_python_binding_rejects_cpu_tensors():
+    import torch
+    import gated_delta_rule_09_gb300 as gdn
+    x = torch.zeros(1, 4, 1, 16)
+    with pytest.raises(TypeError):
+        gdn.gdn_chunk_fwd(x, x, x, torch.zeros(1, 4, 1), torch.zeros(1, 4, 1))
