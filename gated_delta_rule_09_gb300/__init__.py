@@ -2,7 +2,8 @@
 
 The compute runs in libgdn.so (hand-written CUDA for sm_103a) behind the C ABI
 of ``include/gdn.h``; this module only marshals torch CUDA tensors into that
-call.  Importing it loads the library and raises if it is missing.
+call.  The library is loaded on first use, and every entry point raises
+ImportError if it is missing: there is no fallback.
 """
 from __future__ import annotations
 
@@ -14,8 +15,6 @@ from . import _lib
 from ._lib import GdnError, GDN_BF16, GDN_F32  # noqa: F401
 
 _DTYPES = {torch.float32: _lib.GDN_F32, torch.bfloat16: _lib.GDN_BF16}
-
-_lib.load()
 
 
 def _ptr(t):
@@ -33,6 +32,11 @@ def _need_cuda(name, t, dtype=None):
         raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
 
 
+def load():
+    """Load libgdn.so now (raises ImportError if it has not been built)."""
+    return _lib.load()
+
+
 def gdn_chunk_fwd(q, k, v, log_alpha, beta, S0=None, o=None, S_final=None,
                   C=64, cu_seqlens=None, stream=None, want_final_state=True):
     """Chunkwise gated delta rule forward; returns ``(o, S_final)``.
@@ -44,6 +48,7 @@ def gdn_chunk_fwd(q, k, v, log_alpha, beta, S0=None, o=None, S_final=None,
     allocated here.  Runs on ``stream`` (a torch.cuda.Stream, a raw handle, or
     None for the current torch stream).
     """
+    lib = _lib.load()
     if q.dtype not in _DTYPES:
         raise TypeError("q/k/v dtype must be float32 or bfloat16, got %s" % q.dtype)
     for name, t in (("q", q), ("k", k), ("v", v)):
@@ -79,7 +84,7 @@ def gdn_chunk_fwd(q, k, v, log_alpha, beta, S0=None, o=None, S_final=None,
     else:
         handle = int(stream)
     with torch.cuda.device(q.device):
-        st = _lib.load().gdn_chunk_fwd(
+        st = lib.gdn_chunk_fwd(
             _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(S0),
             _ptr(o), _ptr(S_final), N, H, T, dk, dv, int(C), _ptr(cu_seqlens),
             _DTYPES[q.dtype], ctypes.c_void_p(handle))
