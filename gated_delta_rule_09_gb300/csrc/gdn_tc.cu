@@ -1,5 +1,5 @@
 // tcgen05 tensor-core kernel for the chunkwise gated delta rule (bf16 in/out,
-// fp32 state and accumulation) on sm_103a.
+// fp32 state and accumulation, fp16 tensor-core operands) on sm_103a.
 //
 // One CTA (4 warps) owns one (sequence, head, 128-wide d_v tile) and walks the
 // sequence's chunks of C = 64 tokens in order.  The d_v x d_k state slice lives
@@ -13,12 +13,17 @@
 //   T   = (I + A)^{-1}, blocked forward substitution in shared memory  (CUDA cores)
 //   batch 2  W^T = K^T (T diag(beta e^g))^T,  U^T = V^T (T diag(beta))^T
 //   batch 3  S W^T
-//   V_new^T = U^T - S W^T   (bf16 copy, and a copy scaled by e^{g_C - g_j})
+//   V_new^T = U^T - S W^T   (fp16 copy, and a copy scaled by e^{g_C - g_j})
 //   batch 4  O^T_intra = V_new^T P^T,   S <- e^{g_C} S + (V_new * e^{g_C-g})^T K
 //   o_i = e^{g_i} (S Q^T)_i + O_intra_i  -> bf16
 //
 // Every MMA has M = 128 (d_k or the d_v tile on the M side), so each row of a
 // result is one TMEM lane and one thread of the epilogue owns it.  Operands
+// are fp16 (11-bit significand): the bf16 q/k/v tiles are converted in shared
+// memory after they land (exact for |x| < 65504) and every operand written by
+// the epilogues is fp16; accumulation and the state stay fp32.  bf16 operands
+// throughout would leave about 0.03 x RMS of error in o on these workloads, fp16
+// about 0.003.  A value outside the fp16 range raises GDN_DEV_F16_RANGE.  Operands
 // are 128-byte-swizzled shared-memory tiles; q/k/v tiles arrive by TMA (the
 // next chunk's q/k while the current one computes), the rest are written by
 // the epilogue threads.  Every mbarrier wait is bounded: on timeout the CTA
@@ -26,6 +31,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <mutex>
 
 #include "gdn_internal.h"
@@ -45,7 +51,7 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
 constexpr int kKQStage = 32768;                 // 2 d_k-halves x [K rows 0-63 | Q rows 64-127] x 128 B
 constexpr int kOffKQ = 0;                       // 2 stages
 constexpr int kOffV = kOffKQ + 2 * kKQStage;    // 2 d_v-halves x 64 rows x 128 B
-constexpr int kOffSb = kOffV + 16384;           // S (bf16), 2 d_k-halves x 128 rows x 128 B
+constexpr int kOffSb = kOffV + 16384;           // S (fp16), 2 d_k-halves x 128 rows x 128 B
 constexpr int kOffR = kOffSb + 32768;           // Ws | VnT | VnTs  (aliased by A, T, X fp32)
 constexpr int kOffWs = kOffR;
 constexpr int kOffVnT = kOffR + 16384;
@@ -69,21 +75,44 @@ struct Small {
 };
 static_assert(sizeof(Small) <= 2048, "small shared block");
 
-__device__ __forceinline__ uint32_t pack_bf16(float a, float b)
+constexpr float kF16Max = 65504.f;
+
+__device__ __forceinline__ uint32_t pack_f16(float a, float b)
 {
-    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    __half2 h = __floats2half2_rn(a, b);
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
-// Write 8 consecutive values of row r, 16-byte chunk c, of a swizzled tile.
-__device__ __forceinline__ void st_chunk(uint8_t *tile, int r, int c, const float *x)
+// Write 8 consecutive values of row r, 16-byte chunk c, of a swizzled tile as
+// fp16, folding their magnitudes into *amax for the range check.
+__device__ __forceinline__ void st_chunk(uint8_t *tile, int r, int c, const float *x, float *amax)
 {
     uint4 u;
-    u.x = pack_bf16(x[0], x[1]);
-    u.y = pack_bf16(x[2], x[3]);
-    u.z = pack_bf16(x[4], x[5]);
-    u.w = pack_bf16(x[6], x[7]);
+    u.x = pack_f16(x[0], x[1]);
+    u.y = pack_f16(x[2], x[3]);
+    u.z = pack_f16(x[4], x[5]);
+    u.w = pack_f16(x[6], x[7]);
+    float m = *amax;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) m = fmaxf(m, fabsf(x[e]));
+    *amax = m;
     *reinterpret_cast<uint4 *>(tile + sw128(r, c)) = u;
+}
+
+// bf16 -> fp16 for the 8 values of one 16-byte chunk, in place.
+__device__ __forceinline__ void chunk_bf16_to_f16(uint8_t *p, float *amax)
+{
+    uint4 u = *reinterpret_cast<const uint4 *>(p);
+    uint32_t w[4] = {u.x, u.y, u.z, u.w};
+    float m = *amax;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w[e]));
+        m = fmaxf(m, fmaxf(fabsf(f.x), fabsf(f.y)));
+        w[e] = pack_f16(f.x, f.y);
+    }
+    *amax = m;
+    *reinterpret_cast<uint4 *>(p) = make_uint4(w[0], w[1], w[2], w[3]);
 }
 
 __device__ __forceinline__ uint32_t lane_addr(uint32_t tbase, int warp, uint32_t col)
@@ -209,6 +238,7 @@ gdn_tc_kernel(const GdnArgs a, const __grid_constant__ CUtensorMap tm_q,
     load_gates(0);
 
     uint32_t mma_phase = 0;
+    float amax = 0.f;  // largest magnitude this thread converted to fp16
     int c = 0;
     for (; c < nchunks; ++c) {
         const int nc = (int)min((long)kC, len - (long)c * kC);
@@ -245,20 +275,19 @@ gdn_tc_kernel(const GdnArgs a, const __grid_constant__ CUtensorMap tm_q,
         // -------- this chunk's tiles
         if (!wait_or_abort(&s->bar_kq[c & 1], (c >> 1) & 1, s, a.status)) {}
         if (!wait_or_abort(&s->bar_v, c & 1, s, a.status)) {}
-        if (nc < kC) {  // rows past the sequence: zero (they may hold another sequence)
-            for (int idx = tid; idx < (kC - nc) * 8; idx += kThreads) {
-                const int r = nc + idx / 8, cc = idx % 8;
-                const uint4 z = make_uint4(0, 0, 0, 0);
-                *reinterpret_cast<uint4 *>(kq + sw128(r, cc)) = z;
-                *reinterpret_cast<uint4 *>(kq + 16384 + sw128(r, cc)) = z;
-                *reinterpret_cast<uint4 *>(kq + 8192 + sw128(r, cc)) = z;
-                *reinterpret_cast<uint4 *>(kq + 16384 + 8192 + sw128(r, cc)) = z;
-                *reinterpret_cast<uint4 *>(Vt + sw128(r, cc)) = z;
-                *reinterpret_cast<uint4 *>(Vt + 8192 + sw128(r, cc)) = z;
-            }
+        // bf16 -> fp16 in place; rows past the sequence are zeroed (they may
+        // hold another sequence).  Six 64-row tiles: K, Q for both d_k halves,
+        // V for both d_v halves; 8 chunks of 16 B per row.
+        for (int idx = tid; idx < 6 * kC * 8; idx += kThreads) {
+            const int tile = idx / (kC * 8), r = (idx / 8) % kC, cc = idx % 8;
+            uint8_t *base = tile < 4 ? kq + (tile >> 1) * 16384 + (tile & 1) * 8192
+                                     : Vt + (tile - 4) * 8192;
+            uint8_t *p = base + sw128(r, cc);
+            if (r < nc) chunk_bf16_to_f16(p, &amax);
+            else *reinterpret_cast<uint4 *>(p) = make_uint4(0, 0, 0, 0);
         }
 
-        // -------- incoming state: bf16 copy for the MMAs, TMEM <- e^{g_C} S
+        // -------- incoming state: fp16 copy for the MMAs, TMEM <- e^{g_C} S
         {
             const float dC = __expf(gC);
             for (int cb = 0; cb < 4; ++cb) {
@@ -267,7 +296,7 @@ gdn_tc_kernel(const GdnArgs a, const __grid_constant__ CUtensorMap tm_q,
                 tmem_ld_wait();
                 uint8_t *box = Sb + (cb >> 1) * 16384;
 #pragma unroll
-                for (int q = 0; q < 4; ++q) st_chunk(box, tid, (cb & 1) * 4 + q, x + q * 8);
+                for (int q = 0; q < 4; ++q) st_chunk(box, tid, (cb & 1) * 4 + q, x + q * 8, &amax);
 #pragma unroll
                 for (int j = 0; j < 32; ++j) x[j] *= dC;
                 tmem_st32(lane_addr(tbase, warp, kColS + cb * 32), x);
@@ -282,13 +311,13 @@ gdn_tc_kernel(const GdnArgs a, const __grid_constant__ CUtensorMap tm_q,
         // -------- batch 1: [K;Q] K^T  and  S Q^T
         if (tid == 0) {
             tc_fence_after();
-            const uint32_t id = idesc_bf16_f32(128, 64, 0, 0);
+            const uint32_t id = idesc_f16_f32(128, 64, 0, 0);
             const uint32_t kqa = smem_u32(kq), sba = smem_u32(Sb);
             for (int ks = 0; ks < 8; ++ks) {
                 const uint32_t o = (ks >> 2) * 16384 + (ks & 3) * 32;
-                mma_bf16(tbase + kColKQ, sdesc_sw128(kqa + o, 16, 1024),
+                mma_f16kind(tbase + kColKQ, sdesc_sw128(kqa + o, 16, 1024),
                          sdesc_sw128(kqa + o, 16, 1024), id, ks > 0);
-                mma_bf16(tbase + kColSQ, sdesc_sw128(sba + o, 16, 1024),
+                mma_f16kind(tbase + kColSQ, sdesc_sw128(sba + o, 16, 1024),
                          sdesc_sw128(kqa + o + 8192, 16, 1024), id, ks > 0);
             }
             mma_commit(&s->bar_mma);
@@ -297,7 +326,7 @@ gdn_tc_kernel(const GdnArgs a, const __grid_constant__ CUtensorMap tm_q,
         mma_phase ^= 1;
         tc_fence_after();
 
-        // -------- A (fp32, rows 0-63) and P (bf16, rows 64-127)
+        // -------- A (fp32, rows 0-63) and P (fp16, rows 64-127)
         {
             const bool is_k = tid < kC;
             const int i = is_k ? tid : tid - kC;
@@ -320,7 +349,7 @@ gdn_tc_kernel(const GdnArgs a, const __grid_constant__ CUtensorMap tm_q,
                         x[jj] = (j <= i) ? x[jj] * __expf(gi - s->g[j]) : 0.f;
                     }
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) st_chunk(Pm, i, half * 4 + q, x + q * 8);
+                    for (int q = 0; q < 4; ++q) st_chunk(Pm, i, half * 4 + q, x + q * 8, &amax);
                 }
             }
         }
@@ -399,7 +428,7 @@ gdn_tc_kernel(const GdnArgs a, const __grid_constant__ CUtensorMap tm_q,
                     const float sc = first ? s->beta[cc] * s->eg[cc] : s->beta[cc];
                     x[e] = (cc <= j) ? Ts[j * kLdA + cc] * sc : 0.f;
                 }
-                st_chunk(dst, j, q, x);
+                st_chunk(dst, j, q, x, &amax);
             }
         }
         fence_async_smem();
@@ -409,12 +438,12 @@ gdn_tc_kernel(const GdnArgs a, const __grid_constant__ CUtensorMap tm_q,
         // -------- batch 2: W^T = K^T T''^T (A: K as MN-major),  U^T = V^T T'^T
         if (tid == 0) {
             tc_fence_after();
-            const uint32_t idw = idesc_bf16_f32(128, 64, 1, 0);
+            const uint32_t idw = idesc_f16_f32(128, 64, 1, 0);
             const uint32_t kqa = smem_u32(kq), va = smem_u32(Vt);
             for (int ks = 0; ks < 4; ++ks) {
-                mma_bf16(tbase + kColW, sdesc_sw128(kqa + ks * 2048, 16384, 1024),
+                mma_f16kind(tbase + kColW, sdesc_sw128(kqa + ks * 2048, 16384, 1024),
                          sdesc_sw128(smem_u32(Tpp) + ks * 32, 16, 1024), idw, ks > 0);
-                mma_bf16(tbase + kColU, sdesc_sw128(va + ks * 2048, 8192, 1024),
+                mma_f16kind(tbase + kColU, sdesc_sw128(va + ks * 2048, 8192, 1024),
                          sdesc_sw128(smem_u32(Tp) + ks * 32, 16, 1024), idw, ks > 0);
             }
             mma_commit(&s->bar_mma);
@@ -435,7 +464,7 @@ gdn_tc_kernel(const GdnArgs a, const __grid_constant__ CUtensorMap tm_q,
                 tmem_ld32(lane_addr(tbase, warp, kColW + half * 32), x);
                 tmem_ld_wait();
 #pragma unroll
-                for (int q = 0; q < 4; ++q) st_chunk(Ws, tid, half * 4 + q, x + q * 8);
+                for (int q = 0; q < 4; ++q) st_chunk(Ws, tid, half * 4 + q, x + q * 8, &amax);
             }
         }
         fence_async_smem();
@@ -445,11 +474,11 @@ gdn_tc_kernel(const GdnArgs a, const __grid_constant__ CUtensorMap tm_q,
         // -------- batch 3: S W^T
         if (tid == 0) {
             tc_fence_after();
-            const uint32_t id = idesc_bf16_f32(128, 64, 0, 1);
+            const uint32_t id = idesc_f16_f32(128, 64, 0, 1);
             const uint32_t sba = smem_u32(Sb), wsa = smem_u32(Ws);
             for (int ks = 0; ks < 8; ++ks) {
                 const uint32_t o = (ks >> 2) * 16384 + (ks & 3) * 32;
-                mma_bf16(tbase + kColSW, sdesc_sw128(sba + o, 16, 1024),
+                mma_f16kind(tbase + kColSW, sdesc_sw128(sba + o, 16, 1024),
                          sdesc_sw128(wsa + ks * 2048, 8192, 1024), id, ks > 0);
             }
             mma_commit(&s->bar_mma);
@@ -468,11 +497,11 @@ gdn_tc_kernel(const GdnArgs a, const __grid_constant__ CUtensorMap tm_q,
 #pragma unroll
                 for (int j = 0; j < 32; ++j) u[j] -= w[j];
 #pragma unroll
-                for (int q = 0; q < 4; ++q) st_chunk(VnT, tid, half * 4 + q, u + q * 8);
+                for (int q = 0; q < 4; ++q) st_chunk(VnT, tid, half * 4 + q, u + q * 8, &amax);
 #pragma unroll
                 for (int j = 0; j < 32; ++j) u[j] *= s->ekc[half * 32 + j];
 #pragma unroll
-                for (int q = 0; q < 4; ++q) st_chunk(VnTs, tid, half * 4 + q, u + q * 8);
+                for (int q = 0; q < 4; ++q) st_chunk(VnTs, tid, half * 4 + q, u + q * 8, &amax);
             }
         }
         fence_async_smem();
@@ -482,13 +511,13 @@ gdn_tc_kernel(const GdnArgs a, const __grid_constant__ CUtensorMap tm_q,
         // -------- batch 4: O_intra^T = V_new^T P^T;  S += (V_new e^{gC-g})^T K
         if (tid == 0) {
             tc_fence_after();
-            const uint32_t ido = idesc_bf16_f32(128, 64, 0, 0);
-            const uint32_t ids = idesc_bf16_f32(128, 128, 0, 1);
+            const uint32_t ido = idesc_f16_f32(128, 64, 0, 0);
+            const uint32_t ids = idesc_f16_f32(128, 128, 0, 1);
             const uint32_t kqa = smem_u32(kq);
             for (int ks = 0; ks < 4; ++ks) {
-                mma_bf16(tbase + kColO, sdesc_sw128(smem_u32(VnT) + ks * 32, 16, 1024),
+                mma_f16kind(tbase + kColO, sdesc_sw128(smem_u32(VnT) + ks * 32, 16, 1024),
                          sdesc_sw128(smem_u32(Pm) + ks * 32, 16, 1024), ido, ks > 0);
-                mma_bf16(tbase + kColS, sdesc_sw128(smem_u32(VnTs) + ks * 32, 16, 1024),
+                mma_f16kind(tbase + kColS, sdesc_sw128(smem_u32(VnTs) + ks * 32, 16, 1024),
                          sdesc_sw128(kqa + ks * 2048, 16384, 1024), ids, 1);
             }
             mma_commit(&s->bar_mma);
@@ -519,6 +548,8 @@ gdn_tc_kernel(const GdnArgs a, const __grid_constant__ CUtensorMap tm_q,
         __syncthreads();
         if (s->abort_flag) break;
     }
+
+    if (amax > kF16Max) atomicOr(a.status, 0x4u);
 
     // -------- final state, or drain after an abort
     if (!s->abort_flag) {

@@ -150,17 +150,26 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32])
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // ---------------------------------------------------------------- MMA
-// Instruction descriptor, kind::f16 with bf16 A/B and fp32 accumulation.
-// a_mn / b_mn select MN-major (1) instead of K-major (0) operand layout.
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int a_mn, int b_mn)
+// Instruction descriptor for kind::f16 with fp32 accumulation; `ab_fmt` is the
+// A/B element type (0 = f16, 1 = bf16; A and B always share it).  a_mn / b_mn
+// select MN-major (1) instead of K-major (0) operand layout.
+__host__ __device__ constexpr uint32_t idesc_f32acc(int ab_fmt, int M, int N, int a_mn, int b_mn)
 {
-    return (1u << 4)                                 // D format: f32
-           | (1u << 7)                               // A format: bf16
-           | (1u << 10)                              // B format: bf16
+    return (1u << 4)                                     // D format: f32
+           | (static_cast<uint32_t>(ab_fmt) << 7)        // A format
+           | (static_cast<uint32_t>(ab_fmt) << 10)       // B format
            | (static_cast<uint32_t>(a_mn) << 15)     // A major
            | (static_cast<uint32_t>(b_mn) << 16)     // B major
            | (static_cast<uint32_t>(N >> 3) << 17)   // N / 8
            | (static_cast<uint32_t>(M >> 4) << 24);  // M / 16
+}
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int a_mn, int b_mn)
+{
+    return idesc_f32acc(1, M, N, a_mn, b_mn);
+}
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, int a_mn, int b_mn)
+{
+    return idesc_f32acc(0, M, N, a_mn, b_mn);
 }
 
 // Shared-memory matrix descriptor for a 128-byte-swizzled operand.
@@ -179,8 +188,9 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
            | (2ull << 61);    // 128-byte swizzle
 }
 
-// D[tmem] (+)= A[smem desc] * B[smem desc]^T, issued by one thread.
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+// D[tmem] (+)= A[smem desc] * B[smem desc]^T, issued by one thread
+// (kind::f16: 16-bit A/B of the type the instruction descriptor names).
+__device__ __forceinline__ void mma_f16kind(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                          uint32_t idesc, uint32_t accumulate)
 {
     asm volatile(

@@ -52,6 +52,7 @@ typedef enum { GDN_F32 = 0, GDN_BF16 = 1 } gdn_dtype_t;
 /* Device-side status bits returned by gdn_get_device_status(). */
 #define GDN_DEV_BAD_SEQLENS 0x1u /* a cu_seqlens span was negative or past T */
 #define GDN_DEV_WAIT_TIMEOUT 0x2u /* a bounded pipeline wait gave up          */
+#define GDN_DEV_F16_RANGE 0x4u    /* a tensor-core operand left the fp16 range  */
 
 /*
  * gdn_chunk_fwd — forward pass of the gated delta rule, chunkwise.
@@ -84,8 +85,11 @@ typedef enum { GDN_F32 = 0, GDN_BF16 = 1 } gdn_dtype_t;
  *              sequence starts from its own S0[n].  Spans that are negative or
  *              run past T are skipped on the device and raise
  *              GDN_DEV_BAD_SEQLENS (see gdn_get_device_status).
- *   dtype      GDN_F32 or GDN_BF16 (q, k, v and o share it; the arithmetic is
- *              fp32 in either case, with bf16 tensor-core operands for bf16)
+ *   dtype      GDN_F32 or GDN_BF16 (q, k, v and o share it).  fp32 runs in
+ *              fp32 on CUDA cores.  bf16 runs on the tensor cores with fp16
+ *              operands (11-bit significand; bf16 inputs convert exactly for
+ *              |x| < 65504) and fp32 accumulation and state; an operand that
+ *              leaves the fp16 range raises GDN_DEV_F16_RANGE
  *   stream     cudaStream_t to enqueue on
  *
  * Alignment: q, k, v, o must be aligned to 16 bytes; log_alpha, beta, S0 and
