@@ -1,37 +1,47 @@
 // tcgen05 tensor-core kernel for the chunkwise gated delta rule (bf16 in/out,
 // fp32 state and accumulation, fp16 tensor-core operands) on sm_103a.
 //
-// One CTA (4 warps) owns one (sequence, head, 128-wide d_v tile) and walks the
-// sequence's chunks of C = 64 tokens in order.  The d_v x d_k state slice lives
-// in TMEM as an fp32 MMA accumulator for the whole walk.  Per chunk, in the
-// notation of "从零开始的 GDN 推导" (§"UT transform", §"S 的推导", §"O 的推导",
-// §"总结") transposed so that S is d_v x d_k (g = in-chunk cumulative log-decay):
+// Work unit: one (sequence, head, 128-wide d_v tile), walked chunk by chunk
+// (C = 64 tokens).  In the notation of "从零开始的 GDN 推导" (§"UT transform",
+// §"S 的推导", §"O 的推导", §"总结"), transposed so that S is d_v x d_k, with
+// g the in-chunk cumulative sum of log alpha:
 //
-//   batch 1  [K;Q] K^T -> K K^T, Q K^T           S Q^T                (tcgen05)
-//   A   = StrictLower(diag(beta) K K^T * e^{g_i-g_j})                 (CUDA cores)
-//   P   = Lower(Q K^T * e^{g_i-g_j})                                  (CUDA cores)
-//   T   = (I + A)^{-1}, blocked forward substitution in shared memory  (CUDA cores)
-//   batch 2  W^T = K^T (T diag(beta e^g))^T,  U^T = V^T (T diag(beta))^T
-//   batch 3  S W^T
-//   V_new^T = U^T - S W^T   (fp16 copy, and a copy scaled by e^{g_C - g_j})
-//   batch 4  O^T_intra = V_new^T P^T,   S <- e^{g_C} S + (V_new * e^{g_C-g})^T K
-//   o_i = e^{g_i} (S Q^T)_i + O_intra_i  -> bf16
+//   state-independent:  A = StrictLower(diag(beta) K K^T * e^{g_i-g_j})
+//                       P = Lower(Q K^T * e^{g_i-g_j})
+//                       T = (I + A)^{-1}
+//                       W = T diag(beta e^g) K,   T' = T diag(beta)
+//   state chain:        U^T = V^T T'^T,   V_new^T = U^T - S W^T
+//                       O^T = e^{g} (S Q^T) + V_new^T P^T
+//                       S <- e^{g_C} S + (V_new * e^{g_C - g})^T K
 //
-// Every MMA has M = 128 (d_k or the d_v tile on the M side), so each row of a
-// result is one TMEM lane and one thread of the epilogue owns it.  Operands
-// are fp16 (11-bit significand): the bf16 q/k/v tiles are converted in shared
-// memory after they land (exact for |x| < 65504) and every operand written by
-// the epilogues is fp16; accumulation and the state stay fp32.  bf16 operands
-// throughout would leave about 0.03 x RMS of error in o on these workloads, fp16
-// about 0.003.  A value outside the fp16 range raises GDN_DEV_F16_RANGE.  Operands
-// are 128-byte-swizzled shared-memory tiles; q/k/v tiles arrive by TMA (the
-// next chunk's q/k while the current one computes), the rest are written by
-// the epilogue threads.  Every mbarrier wait is bounded: on timeout the CTA
-// sets GDN_DEV_WAIT_TIMEOUT, drains its own TMA copies, frees TMEM and exits.
+// Each unit runs on a cluster of two CTAs on two SMs:
+//
+//  * rank 0, the producer, computes the state-independent part of every chunk
+//    with two 4-warp pipelines (even and odd chunks): TMA loads of the q/k
+//    tiles, [K;Q] K^T on the tensor cores, A and P on the CUDA cores, the
+//    blocked inverse, W^T = K^T (T diag(beta e^g))^T on the tensor cores, and
+//    ships W, P, T' and the decay vectors into the consumer's ring slot with
+//    one distributed-shared-memory bulk copy that completes on the consumer's
+//    mbarrier.
+//  * rank 1, the consumer, keeps the state slice (128 x 128 fp32) in TMEM for
+//    the whole walk.  Warps 0-3 run the state chain (fp16 copy of S, then
+//    V^T T'^T, S W^T and S Q^T, V_new, then V_new^T P^T and the state update);
+//    warps 4-7 convert the next chunk's q/k/v tiles (the consumer's own TMA
+//    loads) and write the previous chunk's outputs from double-buffered TMEM.
+//
+// Every MMA has M = 128, so a result row is one TMEM lane and one epilogue
+// thread.  Operands are fp16 (11-bit significand; bf16 operands would leave
+// about 0.03 x RMS of error in o on the bf16 workloads, fp16 about 0.003):
+// the bf16 q/k/v tiles are converted in shared memory (exact for |x| < 65504)
+// and every epilogue-written operand is fp16; accumulation and the state are
+// fp32.  Values outside the fp16 range raise GDN_DEV_F16_RANGE.  Every wait is
+// bounded: on timeout the CTA raises GDN_DEV_WAIT_TIMEOUT and stops waiting,
+// so the kernel always finishes.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <stddef.h>
 #include <mutex>
 
 #include "gdn_internal.h"
@@ -43,39 +53,55 @@ using namespace sm100;
 
 constexpr int kC = 64;       // chunk length
 constexpr int kDK = 128;     // d_k
-constexpr int kDVT = 128;    // d_v columns per CTA
-constexpr int kThreads = 128;
+constexpr int kDVT = 128;    // d_v columns per unit
+constexpr int kThreads = 256;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
+constexpr float kF16Max = 65504.f;
+constexpr int kLdA = 65;     // padded fp32 row stride of A / T
 
-// shared-memory plan (bytes from a 1024-aligned base)
-constexpr int kKQStage = 32768;                 // 2 d_k-halves x [K rows 0-63 | Q rows 64-127] x 128 B
-constexpr int kOffKQ = 0;                       // 2 stages
-constexpr int kOffV = kOffKQ + 2 * kKQStage;    // 2 d_v-halves x 64 rows x 128 B
-constexpr int kOffSb = kOffV + 16384;           // S (fp16), 2 d_k-halves x 128 rows x 128 B
-constexpr int kOffR = kOffSb + 32768;           // Ws | VnT | VnTs  (aliased by A, T, X fp32)
-constexpr int kOffWs = kOffR;
-constexpr int kOffVnT = kOffR + 16384;
-constexpr int kOffVnTs = kOffR + 32768;
-constexpr int kOffPm = kOffR + 49152;
-constexpr int kOffTpp = kOffPm + 8192;
-constexpr int kOffTp = kOffTpp + 8192;
-constexpr int kOffSmall = kOffTp + 8192;
-constexpr int kLdA = 65;                        // padded fp32 row stride of A / T
-constexpr int kSmemBytes = kOffSmall + 2048 + 1024;  // + small arrays + alignment slack
+// ---- a ring slot: what the producer ships, then the consumer's own tiles
+constexpr int kOutW = 0;           // W^T rows d (MN-major B operand), fp16
+constexpr int kOutP = 16384;       // P rows i (K-major), fp16
+constexpr int kOutTp = 24576;      // T' rows j (K-major), fp16
+constexpr int kOutG = 32768;       // g[64], e^g[64], e^{g_C-g}[64] fp32
+constexpr int kOutBytes = 33792;   // shipped per chunk
+constexpr int kSlotQ = kOutBytes;          // Q, 2 d_k halves x 64 rows x 128 B
+constexpr int kSlotK = kSlotQ + 16384;     // K, same
+constexpr int kSlotV = kSlotK + 16384;     // V, 2 d_v halves (later V_new * e^{g_C-g})
+constexpr int kSlotBytes = kSlotV + 16384;
 
-// tensor-memory columns
-constexpr uint32_t kColKQ = 0, kColSQ = 64, kColW = 128, kColU = 192, kColSW = 256,
-                   kColO = 320, kColS = 384;
+// ---- producer shared memory (per pipeline p = 0, 1)
+constexpr int kPIn = 32768;                        // [K | Q] per d_k half
+constexpr int kPAT = 38912;                        // fp32 A[64][65] | T[64][65] | X[32][33]
+constexpr int kPOffIn = 0;
+constexpr int kPOffOut = kPOffIn + 2 * kPIn;
+constexpr int kPOffAT = kPOffOut + 2 * kOutBytes;
+constexpr int kPOffSmall = kPOffAT + 2 * kPAT;
+// ---- consumer shared memory
+constexpr int kCOffSb = 2 * kSlotBytes;            // S as fp16, 2 d_k halves x 128 rows
+constexpr int kCOffVnT = kCOffSb + 32768;          // V_new^T rows v (K-major), fp16
+constexpr int kCOffSmall = kCOffVnT + 16384;
+constexpr int kSmallBytes = 2048;
+constexpr int kSmemBytes =
+    (kCOffSmall > kPOffSmall ? kCOffSmall : kPOffSmall) + kSmallBytes + 1024;
 
-struct Small {
-    float g[kC], eg[kC], ekc[kC], beta[kC], scan[kC];
-    uint64_t bar_kq[2], bar_v, bar_mma;
+struct PSmall {
+    float scan[2][kC], beta[2][kC];
+    uint64_t tma_in[2], mma[2], src_free[2], slot_empty[2];
     uint32_t tmem;
     int abort_flag;
 };
-static_assert(sizeof(Small) <= 2048, "small shared block");
+struct CSmall {
+    float egc[2][kC];
+    uint64_t full[2], tma[2], conv[2], egc_full[2], mma1, mma2, out_full[2], out_done[2];
+    uint32_t tmem;
+    int abort_flag;
+};
+static_assert(sizeof(PSmall) <= kSmallBytes && sizeof(CSmall) <= kSmallBytes, "small blocks");
+static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 
-constexpr float kF16Max = 65504.f;
+// consumer TMEM columns (512): S W^T | U^T | S Q^T x2 | O_intra^T x2 | S
+constexpr uint32_t kColSW = 0, kColU = 64, kColSQ = 128, kColO = 256, kColS = 384;
 
 __device__ __forceinline__ uint32_t pack_f16(float a, float b)
 {
@@ -83,8 +109,8 @@ __device__ __forceinline__ uint32_t pack_f16(float a, float b)
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
-// Write 8 consecutive values of row r, 16-byte chunk c, of a swizzled tile as
-// fp16, folding their magnitudes into *amax for the range check.
+// 8 values -> fp16 into 16-byte chunk c of row r of a swizzled tile; their
+// magnitudes fold into *amax for the range check.
 __device__ __forceinline__ void st_chunk(uint8_t *tile, int r, int c, const float *x, float *amax)
 {
     uint4 u;
@@ -99,7 +125,7 @@ __device__ __forceinline__ void st_chunk(uint8_t *tile, int r, int c, const floa
     *reinterpret_cast<uint4 *>(tile + sw128(r, c)) = u;
 }
 
-// bf16 -> fp16 for the 8 values of one 16-byte chunk, in place.
+// bf16 -> fp16 in place for one 16-byte chunk.
 __device__ __forceinline__ void chunk_bf16_to_f16(uint8_t *p, float *amax)
 {
     uint4 u = *reinterpret_cast<const uint4 *>(p);
@@ -115,317 +141,245 @@ __device__ __forceinline__ void chunk_bf16_to_f16(uint8_t *p, float *amax)
     *reinterpret_cast<uint4 *>(p) = make_uint4(w[0], w[1], w[2], w[3]);
 }
 
-__device__ __forceinline__ uint32_t lane_addr(uint32_t tbase, int warp, uint32_t col)
+// Convert `ntiles` 64-row x 128-byte tiles in place; rows at or past `nc` are
+// zeroed (they may belong to another sequence).
+template <int NT>
+__device__ __forceinline__ void convert_tiles(uint8_t *const (&tiles)[NT], int nc, int t,
+                                              float *amax)
 {
-    return tbase + (static_cast<uint32_t>(warp * 32) << 16) + col;
+    for (int idx = t; idx < NT * kC * 8; idx += 128) {
+        const int tile = idx / (kC * 8), r = (idx >> 3) & (kC - 1), cc = idx & 7;
+        uint8_t *p = tiles[tile] + sw128(r, cc);
+        if (r < nc) chunk_bf16_to_f16(p, amax);
+        else *reinterpret_cast<uint4 *>(p) = make_uint4(0, 0, 0, 0);
+    }
 }
 
-__device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, Small *s,
-                                              unsigned int *status)
+__device__ __forceinline__ uint32_t lane_addr(uint32_t tbase, int quad, uint32_t col)
 {
-    if (mbar_wait(bar, parity, kWaitLimitNs)) return true;
-    s->abort_flag = 1;
-    atomicOr(status, 0x2u);
-    return false;
+    return tbase + (static_cast<uint32_t>(quad * 32) << 16) + col;
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
-gdn_tc_kernel(const GdnArgs a, const __grid_constant__ CUtensorMap tm_q,
-              const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v)
+// Bounded wait; once this CTA has given up on one wait, every later wait
+// returns immediately so the kernel winds down.
+__device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, bool cluster_scope,
+                                         volatile int *abort_flag, unsigned int *status)
 {
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *sm = reinterpret_cast<uint8_t *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    Small *s = reinterpret_cast<Small *>(sm + kOffSmall);
-    float *As = reinterpret_cast<float *>(sm + kOffR);            // [64][65]
-    float *Ts = As + kC * kLdA;                                    // [64][65]
-    float *Xs = Ts + kC * kLdA;                                    // [32][33]
-    uint8_t *Sb = sm + kOffSb, *Vt = sm + kOffV, *Ws = sm + kOffWs, *VnT = sm + kOffVnT,
-            *VnTs = sm + kOffVnTs, *Pm = sm + kOffPm, *Tpp = sm + kOffTpp, *Tp = sm + kOffTp;
+    if (*abort_flag) return false;
+    if (cluster_scope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+        if (cluster_scope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity))
+            return true;
+        if (*abort_flag) return false;
+        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            *abort_flag = 1;
+            atomicOr(status, 0x2u);
+            return false;
+        }
+    }
+}
 
+// ======================================================================
+// producer: the state-independent part of every chunk
+// ======================================================================
+__device__ __forceinline__ void producer(const GdnArgs &a, const CUtensorMap *tm_q,
+                                         const CUtensorMap *tm_k, uint8_t *sm, uint32_t tbase,
+                                         long start, long len, int nchunks, int h)
+{
+    PSmall *s = reinterpret_cast<PSmall *>(sm + kPOffSmall);
+    volatile int *abort_flag = &s->abort_flag;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int vt = blockIdx.x, h = blockIdx.y, n = blockIdx.z;
-    const int H = a.H, dv = a.dv;
-    const int v0 = vt * kDVT;
+    const int p = warp >> 2, quad = warp & 3, t = tid & 127;
+    const uint32_t bar_id = 1 + p;
+    uint8_t *in = sm + kPOffIn + p * kPIn;
+    uint8_t *out = sm + kPOffOut + p * kOutBytes;
+    float *As = reinterpret_cast<float *>(sm + kPOffAT + p * kPAT);
+    float *Ts = As + kC * kLdA;
+    float *Xs = Ts + kC * kLdA;
+    uint8_t *Tpp = reinterpret_cast<uint8_t *>(As);  // written once the inverse is done
+    float *gout = reinterpret_cast<float *>(out + kOutG);
+    const uint32_t tcol = tbase + p * 128;           // [K;Q]K^T at +0, W^T at +64
+    const uint32_t r_full =
+        mapa_shared(sm + kCOffSmall + offsetof(CSmall, full) + p * sizeof(uint64_t), 1);
+    const uint32_t r_slot = mapa_shared(sm + p * kSlotBytes, 1);
+    float amax = 0.f;
 
-    long start = 0, len = 0;
-    bool bad = false;
-    if (a.cu_seqlens) {
-        const int s0 = a.cu_seqlens[n], e0 = a.cu_seqlens[n + 1];
-        if (s0 < 0 || e0 < s0 || e0 > a.T) bad = true;
-        else { start = s0; len = e0 - s0; }
-    } else {
-        start = (long)n * a.T;
-        len = a.T;
-    }
-    if (bad) {  // uniform across the CTA: nothing allocated yet
-        if (tid == 0) atomicOr(a.status, 0x1u);
-        return;
-    }
-    const int nchunks = (int)((len + kC - 1) / kC);
-
-    if (warp == 0) {
-        tmem_alloc(&s->tmem, 512);
-        tmem_relinquish();
-    }
-    if (tid == 0) {
-        mbar_init(&s->bar_kq[0], 1);
-        mbar_init(&s->bar_kq[1], 1);
-        mbar_init(&s->bar_v, 1);
-        mbar_init(&s->bar_mma, 1);
-        s->abort_flag = 0;
-        fence_mbar_init();
-        prefetch_tensormap(&tm_q);
-        prefetch_tensormap(&tm_k);
-        prefetch_tensormap(&tm_v);
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tbase = s->tmem;
-
-    // q/k tiles of chunk c into stage (c & 1); v tile into the single V buffer
-    auto issue_kq = [&](int c) {
-        uint8_t *kq = sm + kOffKQ + (c & 1) * kKQStage;
+    auto issue_in = [&](int c) {
         const int z = (int)(start + (long)c * kC);
-        mbar_arrive_expect_tx(&s->bar_kq[c & 1], 4 * 8192);
+        mbar_arrive_expect_tx(&s->tma_in[p], 4 * 8192);
         for (int b = 0; b < 2; ++b) {
-            tma_load_3d(kq + b * 16384, &tm_k, &s->bar_kq[c & 1], b * 64, h, z);
-            tma_load_3d(kq + b * 16384 + 8192, &tm_q, &s->bar_kq[c & 1], b * 64, h, z);
+            tma_load_3d(in + b * 16384, tm_k, &s->tma_in[p], b * 64, h, z);
+            tma_load_3d(in + b * 16384 + 8192, tm_q, &s->tma_in[p], b * 64, h, z);
         }
     };
-    auto issue_v = [&](int c) {
-        const int z = (int)(start + (long)c * kC);
-        mbar_arrive_expect_tx(&s->bar_v, 2 * 8192);
-        for (int b = 0; b < 2; ++b)
-            tma_load_3d(Vt + b * 8192, &tm_v, &s->bar_v, v0 + b * 64, h, z);
-    };
-    // outstanding-copy bookkeeping (thread 0 only) for draining on abort
-    int kq_issued = 0, v_issued = 0;
-    if (tid == 0 && nchunks > 0) {
-        issue_kq(0);
-        issue_v(0);
-        kq_issued = 1;
-        v_issued = 1;
-    }
-
-    // initial state into the TMEM accumulator (lane = d_v row)
-    {
-        const float *src = a.S0 ? a.S0 + (((size_t)n * H + h) * dv + v0 + tid) * kDK : nullptr;
-        for (int cb = 0; cb < 4; ++cb) {
-            float x[32];
-#pragma unroll
-            for (int j = 0; j < 32; ++j) x[j] = src ? src[cb * 32 + j] : 0.f;
-            tmem_st32(lane_addr(tbase, warp, kColS + cb * 32), x);
-        }
-        tmem_st_wait();
-    }
-
-    // gates of the next chunk, prefetched into registers by threads 0..63
     float la_next = 0.f, b_next = 0.f;
     auto load_gates = [&](int c) {
         la_next = 0.f;
         b_next = 0.f;
-        if (tid < kC && c < nchunks) {
-            const long t = (long)c * kC + tid;
-            if (t < len) {
-                const size_t gi = (size_t)(start + t) * H + h;
+        if (t < kC && c < nchunks) {
+            const long tt = (long)c * kC + t;
+            if (tt < len) {
+                const size_t gi = (size_t)(start + tt) * a.H + h;
                 la_next = a.log_alpha[gi];
                 b_next = a.beta[gi];
             }
         }
     };
-    load_gates(0);
+    if (p < nchunks && t == 0) issue_in(p);
+    load_gates(p);
 
-    uint32_t mma_phase = 0;
-    float amax = 0.f;  // largest magnitude this thread converted to fp16
-    int c = 0;
-    for (; c < nchunks; ++c) {
+    int k = 0;
+    for (int c = p; c < nchunks; c += 2, ++k) {
         const int nc = (int)min((long)kC, len - (long)c * kC);
-        const long tok0 = start + (long)c * kC;
-        uint8_t *kq = sm + kOffKQ + (c & 1) * kKQStage;
+        // the consumer has received this buffer's previous contents
+        wait_bar(&s->src_free[p], (k + 1) & 1, true, abort_flag, a.status);
 
-        // -------- decay: g = inclusive cumulative sum of log alpha (padding adds 0)
+        // decay: g = inclusive cumulative sum of log alpha (padding adds 0)
         const float la = la_next, bt = b_next;
-        load_gates(c + 1);
-        if (tid < kC) {
+        load_gates(c + 2);
+        if (t < kC) {
             float x = la;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
                 const float y = __shfl_up_sync(0xffffffffu, x, o);
                 if (lane >= o) x += y;
             }
-            s->scan[tid] = x;
-            s->beta[tid] = bt;
+            s->scan[p][t] = x;
+            s->beta[p][t] = bt;
         }
-        __syncthreads();
-        if (tid < kC) s->g[tid] = s->scan[tid] + (tid >= 32 ? s->scan[31] : 0.f);
-        __syncthreads();
-        const float gC = s->g[kC - 1];
-        if (tid < kC) {
-            s->eg[tid] = __expf(s->g[tid]);
-            s->ekc[tid] = __expf(gC - s->g[tid]);
-        }
-        // next chunk's q/k into the other stage (free since the previous chunk ended)
-        if (tid == 0 && c + 1 < nchunks) {
-            issue_kq(c + 1);
-            ++kq_issued;
+        named_sync(bar_id, 128);
+        if (t < kC) gout[t] = s->scan[p][t] + (t >= 32 ? s->scan[p][31] : 0.f);
+        named_sync(bar_id, 128);
+        const float gC = gout[kC - 1];
+        if (t < kC) {
+            gout[kC + t] = __expf(gout[t]);
+            gout[2 * kC + t] = __expf(gC - gout[t]);
         }
 
-        // -------- this chunk's tiles
-        if (!wait_or_abort(&s->bar_kq[c & 1], (c >> 1) & 1, s, a.status)) {}
-        if (!wait_or_abort(&s->bar_v, c & 1, s, a.status)) {}
-        // bf16 -> fp16 in place; rows past the sequence are zeroed (they may
-        // hold another sequence).  Six 64-row tiles: K, Q for both d_k halves,
-        // V for both d_v halves; 8 chunks of 16 B per row.
-        for (int idx = tid; idx < 6 * kC * 8; idx += kThreads) {
-            const int tile = idx / (kC * 8), r = (idx / 8) % kC, cc = idx % 8;
-            uint8_t *base = tile < 4 ? kq + (tile >> 1) * 16384 + (tile & 1) * 8192
-                                     : Vt + (tile - 4) * 8192;
-            uint8_t *p = base + sw128(r, cc);
-            if (r < nc) chunk_bf16_to_f16(p, &amax);
-            else *reinterpret_cast<uint4 *>(p) = make_uint4(0, 0, 0, 0);
-        }
-
-        // -------- incoming state: fp16 copy for the MMAs, TMEM <- e^{g_C} S
+        // q/k tiles -> fp16
+        wait_bar(&s->tma_in[p], k & 1, false, abort_flag, a.status);
         {
-            const float dC = __expf(gC);
-            for (int cb = 0; cb < 4; ++cb) {
-                float x[32];
-                tmem_ld32(lane_addr(tbase, warp, kColS + cb * 32), x);
-                tmem_ld_wait();
-                uint8_t *box = Sb + (cb >> 1) * 16384;
-#pragma unroll
-                for (int q = 0; q < 4; ++q) st_chunk(box, tid, (cb & 1) * 4 + q, x + q * 8, &amax);
-#pragma unroll
-                for (int j = 0; j < 32; ++j) x[j] *= dC;
-                tmem_st32(lane_addr(tbase, warp, kColS + cb * 32), x);
-            }
-            tmem_st_wait();
+            uint8_t *const tiles[4] = {in, in + 8192, in + 16384, in + 16384 + 8192};
+            convert_tiles<4>(tiles, nc, t, &amax);
         }
         fence_async_smem();
         tc_fence_before();
-        __syncthreads();
-        if (s->abort_flag) break;
+        named_sync(bar_id, 128);
 
-        // -------- batch 1: [K;Q] K^T  and  S Q^T
-        if (tid == 0) {
+        // [K;Q] K^T: lanes 0-63 K K^T, lanes 64-127 Q K^T
+        if (t == 0) {
             tc_fence_after();
             const uint32_t id = idesc_f16_f32(128, 64, 0, 0);
-            const uint32_t kqa = smem_u32(kq), sba = smem_u32(Sb);
+            const uint32_t ia = smem_u32(in);
             for (int ks = 0; ks < 8; ++ks) {
                 const uint32_t o = (ks >> 2) * 16384 + (ks & 3) * 32;
-                mma_f16kind(tbase + kColKQ, sdesc_sw128(kqa + o, 16, 1024),
-                         sdesc_sw128(kqa + o, 16, 1024), id, ks > 0);
-                mma_f16kind(tbase + kColSQ, sdesc_sw128(sba + o, 16, 1024),
-                         sdesc_sw128(kqa + o + 8192, 16, 1024), id, ks > 0);
+                mma_f16kind(tcol, sdesc_sw128(ia + o, 16, 1024), sdesc_sw128(ia + o, 16, 1024), id,
+                            ks > 0);
             }
-            mma_commit(&s->bar_mma);
+            mma_commit(&s->mma[p]);
         }
-        wait_or_abort(&s->bar_mma, mma_phase, s, a.status);
-        mma_phase ^= 1;
+        wait_bar(&s->mma[p], 0, false, abort_flag, a.status);
         tc_fence_after();
 
-        // -------- A (fp32, rows 0-63) and P (fp16, rows 64-127)
+        // A (fp32, rows 0-63) and P (fp16, rows 64-127)
         {
-            const bool is_k = tid < kC;
-            const int i = is_k ? tid : tid - kC;
-            const float gi = s->g[i];
-            const float bi = s->beta[i];
+            const bool is_k = t < kC;
+            const int i = is_k ? t : t - kC;
+            const float gi = gout[i], bi = s->beta[p][i];
             float x[32];
             for (int half = 0; half < 2; ++half) {
-                tmem_ld32(lane_addr(tbase, warp, kColKQ + half * 32), x);
+                tmem_ld32(lane_addr(tcol, quad, half * 32), x);
                 tmem_ld_wait();
                 if (is_k) {
 #pragma unroll
                     for (int jj = 0; jj < 32; ++jj) {
                         const int j = half * 32 + jj;
-                        As[i * kLdA + j] = (j < i) ? bi * x[jj] * __expf(gi - s->g[j]) : 0.f;
+                        As[i * kLdA + j] = (j < i) ? bi * x[jj] * __expf(gi - gout[j]) : 0.f;
                     }
                 } else {
 #pragma unroll
                     for (int jj = 0; jj < 32; ++jj) {
                         const int j = half * 32 + jj;
-                        x[jj] = (j <= i) ? x[jj] * __expf(gi - s->g[j]) : 0.f;
+                        x[jj] = (j <= i) ? x[jj] * __expf(gi - gout[j]) : 0.f;
                     }
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) st_chunk(Pm, i, half * 4 + q, x + q * 8, &amax);
+                    for (int q = 0; q < 4; ++q)
+                        st_chunk(out + kOutP, i, half * 4 + q, x + q * 8, &amax);
                 }
             }
         }
-        fence_async_smem();
         tc_fence_before();
-        __syncthreads();
+        named_sync(bar_id, 128);
 
-        // -------- T = (I + A)^{-1}
-        // (1) the four 16x16 diagonal blocks, one warp each: lane l < 16 owns
-        //     column l of its block and substitutes forward down the rows.
+        // T = (I + A)^{-1}
+        // (1) 16x16 diagonal blocks: warp `quad` owns block `quad`, lane l < 16
+        //     owns column l and substitutes forward down the rows.
         {
-            const int b = warp, l = lane;
-            float t[16];
+            const int b = quad, l = lane;
+            float tv[16];
 #pragma unroll
-            for (int r = 0; r < 16; ++r) t[r] = (r == l) ? 1.f : 0.f;
+            for (int r = 0; r < 16; ++r) tv[r] = (r == l) ? 1.f : 0.f;
 #pragma unroll
             for (int r = 1; r < 16; ++r) {
                 float acc = 0.f;
 #pragma unroll
                 for (int m = 0; m < r; ++m)
-                    if (m >= l) acc = fmaf(As[(16 * b + r) * kLdA + 16 * b + m], t[m], acc);
-                if (r > l) t[r] = -acc;
+                    if (m >= l) acc = fmaf(As[(16 * b + r) * kLdA + 16 * b + m], tv[m], acc);
+                if (r > l) tv[r] = -acc;
             }
             if (l < 16) {
 #pragma unroll
-                for (int r = 0; r < 16; ++r) Ts[(16 * b + r) * kLdA + 16 * b + l] = t[r];
+                for (int r = 0; r < 16; ++r) Ts[(16 * b + r) * kLdA + 16 * b + l] = tv[r];
             }
         }
-        __syncthreads();
-        // (2) 16 -> 32: T[1,0] = -T11 (A10 T00) for the block pairs (0,1), (2,3)
-        for (int idx = tid; idx < 512; idx += kThreads) {
-            const int p = idx >> 8, r = (idx >> 4) & 15, cc = idx & 15;
-            const int R = 16 * (2 * p + 1), Cc = 32 * p;
+        named_sync(bar_id, 128);
+        // (2) 16 -> 32: T[1,0] = -T11 (A10 T00) for block pairs (0,1) and (2,3)
+        for (int idx = t; idx < 512; idx += 128) {
+            const int pp = idx >> 8, r = (idx >> 4) & 15, cc = idx & 15;
+            const int R = 16 * (2 * pp + 1), Cc = 32 * pp;
             float acc = 0.f;
             for (int m = cc; m < 16; ++m)
                 acc = fmaf(As[(R + r) * kLdA + Cc + m], Ts[(Cc + m) * kLdA + Cc + cc], acc);
-            Xs[p * 16 * 17 + r * 17 + cc] = acc;
+            Xs[pp * 16 * 17 + r * 17 + cc] = acc;
         }
-        __syncthreads();
-        for (int idx = tid; idx < 512; idx += kThreads) {
-            const int p = idx >> 8, r = (idx >> 4) & 15, cc = idx & 15;
-            const int R = 16 * (2 * p + 1), Cc = 32 * p;
+        named_sync(bar_id, 128);
+        for (int idx = t; idx < 512; idx += 128) {
+            const int pp = idx >> 8, r = (idx >> 4) & 15, cc = idx & 15;
+            const int R = 16 * (2 * pp + 1), Cc = 32 * pp;
             float acc = 0.f;
             for (int m = 0; m <= r; ++m)
-                acc = fmaf(Ts[(R + r) * kLdA + R + m], Xs[p * 16 * 17 + m * 17 + cc], acc);
+                acc = fmaf(Ts[(R + r) * kLdA + R + m], Xs[pp * 16 * 17 + m * 17 + cc], acc);
             Ts[(R + r) * kLdA + Cc + cc] = -acc;
         }
-        __syncthreads();
+        named_sync(bar_id, 128);
         // (3) 32 -> 64: T[32:64, 0:32] = -T2 (A21 T1)
-        for (int idx = tid; idx < 1024; idx += kThreads) {
+        for (int idx = t; idx < 1024; idx += 128) {
             const int r = idx >> 5, cc = idx & 31;
             float acc = 0.f;
-            for (int m = cc; m < 32; ++m)
-                acc = fmaf(As[(32 + r) * kLdA + m], Ts[m * kLdA + cc], acc);
+            for (int m = cc; m < 32; ++m) acc = fmaf(As[(32 + r) * kLdA + m], Ts[m * kLdA + cc], acc);
             Xs[r * 33 + cc] = acc;
         }
-        __syncthreads();
-        for (int idx = tid; idx < 1024; idx += kThreads) {
+        named_sync(bar_id, 128);
+        for (int idx = t; idx < 1024; idx += 128) {
             const int r = idx >> 5, cc = idx & 31;
             float acc = 0.f;
             for (int m = 0; m <= r; ++m)
                 acc = fmaf(Ts[(32 + r) * kLdA + 32 + m], Xs[m * 33 + cc], acc);
             Ts[(32 + r) * kLdA + cc] = -acc;
         }
-        __syncthreads();
-        // T'' = T diag(beta e^g) (rows 0-63 by threads 0-63), T' = T diag(beta) (threads 64-127)
+        named_sync(bar_id, 128);
+        // T'' = T diag(beta e^g) (local, over A), T' = T diag(beta) (shipped)
         {
-            const bool first = tid < kC;
-            const int j = first ? tid : tid - kC;
-            uint8_t *dst = first ? Tpp : Tp;
+            const bool first = t < kC;
+            const int j = first ? t : t - kC;
+            uint8_t *dst = first ? Tpp : out + kOutTp;
             float x[8];
             for (int q = 0; q < 8; ++q) {
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
                     const int cc = q * 8 + e;
-                    const float sc = first ? s->beta[cc] * s->eg[cc] : s->beta[cc];
+                    const float sc = first ? s->beta[p][cc] * gout[kC + cc] : s->beta[p][cc];
                     x[e] = (cc <= j) ? Ts[j * kLdA + cc] * sc : 0.f;
                 }
                 st_chunk(dst, j, q, x, &amax);
@@ -433,147 +387,342 @@ gdn_tc_kernel(const GdnArgs a, const __grid_constant__ CUtensorMap tm_q,
         }
         fence_async_smem();
         tc_fence_before();
-        __syncthreads();
+        named_sync(bar_id, 128);
 
-        // -------- batch 2: W^T = K^T T''^T (A: K as MN-major),  U^T = V^T T'^T
-        if (tid == 0) {
+        // W^T = K^T T''^T  (A = K read MN-major over the two d_k halves)
+        if (t == 0) {
             tc_fence_after();
             const uint32_t idw = idesc_f16_f32(128, 64, 1, 0);
-            const uint32_t kqa = smem_u32(kq), va = smem_u32(Vt);
-            for (int ks = 0; ks < 4; ++ks) {
-                mma_f16kind(tbase + kColW, sdesc_sw128(kqa + ks * 2048, 16384, 1024),
-                         sdesc_sw128(smem_u32(Tpp) + ks * 32, 16, 1024), idw, ks > 0);
-                mma_f16kind(tbase + kColU, sdesc_sw128(va + ks * 2048, 8192, 1024),
-                         sdesc_sw128(smem_u32(Tp) + ks * 32, 16, 1024), idw, ks > 0);
-            }
-            mma_commit(&s->bar_mma);
+            const uint32_t ia = smem_u32(in), tp = smem_u32(Tpp);
+            for (int ks = 0; ks < 4; ++ks)
+                mma_f16kind(tcol + 64, sdesc_sw128(ia + ks * 2048, 16384, 1024),
+                            sdesc_sw128(tp + ks * 32, 16, 1024), idw, ks > 0);
+            mma_commit(&s->mma[p]);
         }
-        wait_or_abort(&s->bar_mma, mma_phase, s, a.status);
-        mma_phase ^= 1;
+        wait_bar(&s->mma[p], 1, false, abort_flag, a.status);
         tc_fence_after();
-        // V buffer is free: fetch the next chunk's values
-        if (tid == 0 && c + 1 < nchunks) {
-            issue_v(c + 1);
-            ++v_issued;
-        }
+        // the q/k buffer is free: fetch the pipeline's next chunk
+        if (t == 0 && c + 2 < nchunks && !*abort_flag) issue_in(c + 2);
 
-        // -------- W^T rows (lane = d) -> Ws as the MN-major B operand of S W^T
+        // W^T rows (lane = d) -> MN-major B operand of S W^T
         {
             float x[32];
             for (int half = 0; half < 2; ++half) {
-                tmem_ld32(lane_addr(tbase, warp, kColW + half * 32), x);
+                tmem_ld32(lane_addr(tcol + 64, quad, half * 32), x);
                 tmem_ld_wait();
 #pragma unroll
-                for (int q = 0; q < 4; ++q) st_chunk(Ws, tid, half * 4 + q, x + q * 8, &amax);
+                for (int q = 0; q < 4; ++q)
+                    st_chunk(out + kOutW, t, half * 4 + q, x + q * 8, &amax);
             }
         }
         fence_async_smem();
         tc_fence_before();
-        __syncthreads();
+        named_sync(bar_id, 128);
 
-        // -------- batch 3: S W^T
-        if (tid == 0) {
-            tc_fence_after();
-            const uint32_t id = idesc_f16_f32(128, 64, 0, 1);
-            const uint32_t sba = smem_u32(Sb), wsa = smem_u32(Ws);
-            for (int ks = 0; ks < 8; ++ks) {
-                const uint32_t o = (ks >> 2) * 16384 + (ks & 3) * 32;
-                mma_f16kind(tbase + kColSW, sdesc_sw128(sba + o, 16, 1024),
-                         sdesc_sw128(wsa + ks * 2048, 8192, 1024), id, ks > 0);
+        // ship W, P, T' and the decay vectors once the consumer's slot is free
+        if (t == 0) {
+            if (wait_bar(&s->slot_empty[p], (k + 1) & 1, true, abort_flag, a.status)) {
+                mbar_arrive_expect_tx_remote(r_full, kOutBytes);
+                bulk_copy_to_peer(r_slot, out, kOutBytes, r_full);
             }
-            mma_commit(&s->bar_mma);
         }
-        wait_or_abort(&s->bar_mma, mma_phase, s, a.status);
-        mma_phase ^= 1;
-        tc_fence_after();
+    }
+    if (amax > kF16Max) atomicOr(a.status, 0x4u);
+}
 
-        // -------- V_new^T = U^T - S W^T  (row v = tid)
-        {
-            float u[32], w[32];
-            for (int half = 0; half < 2; ++half) {
-                tmem_ld32(lane_addr(tbase, warp, kColU + half * 32), u);
-                tmem_ld32(lane_addr(tbase, warp, kColSW + half * 32), w);
+// ======================================================================
+// consumer: the state chain and the outputs
+// ======================================================================
+__device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm_q,
+                                         const CUtensorMap *tm_k, const CUtensorMap *tm_v,
+                                         uint8_t *sm, uint32_t tbase, long start, long len,
+                                         int nchunks, int h, int n, int v0)
+{
+    CSmall *s = reinterpret_cast<CSmall *>(sm + kCOffSmall);
+    volatile int *abort_flag = &s->abort_flag;
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int quad = warp & 3;
+    const int H = a.H, dv = a.dv;
+    uint8_t *Sb = sm + kCOffSb, *VnT = sm + kCOffVnT;
+    const uint32_t r_src_free = mapa_shared(sm + kPOffSmall + offsetof(PSmall, src_free), 0);
+    const uint32_t r_slot_empty = mapa_shared(sm + kPOffSmall + offsetof(PSmall, slot_empty), 0);
+    float amax = 0.f;
+
+    auto issue_qkv = [&](int c) {
+        uint8_t *slot = sm + (c & 1) * kSlotBytes;
+        const int z = (int)(start + (long)c * kC);
+        mbar_arrive_expect_tx(&s->tma[c & 1], 6 * 8192);
+        for (int b = 0; b < 2; ++b) {
+            tma_load_3d(slot + kSlotQ + b * 8192, tm_q, &s->tma[c & 1], b * 64, h, z);
+            tma_load_3d(slot + kSlotK + b * 8192, tm_k, &s->tma[c & 1], b * 64, h, z);
+            tma_load_3d(slot + kSlotV + b * 8192, tm_v, &s->tma[c & 1], v0 + b * 64, h, z);
+        }
+    };
+
+    if (tid < 128) {
+        // ---------------- state chain (warps 0-3); thread t owns state row v0 + t
+        const int t = tid;
+        if (t == 0) {
+            if (nchunks > 0) issue_qkv(0);
+            if (nchunks > 1) issue_qkv(1);
+        }
+        {   // initial state -> TMEM
+            const float *src = a.S0 ? a.S0 + (((size_t)n * H + h) * dv + v0 + t) * kDK : nullptr;
+            for (int cb = 0; cb < 4; ++cb) {
+                float x[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) x[j] = src ? src[cb * 32 + j] : 0.f;
+                tmem_st32(lane_addr(tbase, quad, kColS + cb * 32), x);
+            }
+            tmem_st_wait();
+        }
+        for (int c = 0; c < nchunks; ++c) {
+            const int sl = c & 1, kk = c >> 1;
+            uint8_t *slot = sm + sl * kSlotBytes;
+            const float *gs = reinterpret_cast<const float *>(slot + kOutG);
+            wait_bar(&s->full[sl], kk & 1, true, abort_flag, a.status);
+            wait_bar(&s->conv[sl], kk & 1, false, abort_flag, a.status);
+            wait_bar(&s->out_done[sl], (kk + 1) & 1, false, abort_flag, a.status);
+            if (t == 0) mbar_arrive_remote(r_src_free + sl * sizeof(uint64_t));
+            if (t < kC) {
+                s->egc[sl][t] = gs[kC + t];
+                mbar_arrive(&s->egc_full[sl]);
+            }
+            const float gC = gs[kC - 1];
+
+            // incoming state: fp16 copy for the MMAs, TMEM <- e^{g_C} S
+            {
+                const float dC = __expf(gC);
+                for (int cb = 0; cb < 4; ++cb) {
+                    float x[32];
+                    tmem_ld32(lane_addr(tbase, quad, kColS + cb * 32), x);
+                    tmem_ld_wait();
+                    uint8_t *box = Sb + (cb >> 1) * 16384;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        st_chunk(box, t, (cb & 1) * 4 + q, x + q * 8, &amax);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) x[j] *= dC;
+                    tmem_st32(lane_addr(tbase, quad, kColS + cb * 32), x);
+                }
+                tmem_st_wait();
+            }
+            fence_async_smem();
+            tc_fence_before();
+            named_sync(1, 128);
+
+            // U^T = V^T T'^T;  S W^T;  S Q^T
+            if (t == 0) {
+                tc_fence_after();
+                const uint32_t id_u = idesc_f16_f32(128, 64, 1, 0);
+                const uint32_t id_w = idesc_f16_f32(128, 64, 0, 1);
+                const uint32_t id_q = idesc_f16_f32(128, 64, 0, 0);
+                const uint32_t sa = smem_u32(slot), sba = smem_u32(Sb);
+                for (int ks = 0; ks < 4; ++ks)
+                    mma_f16kind(tbase + kColU, sdesc_sw128(sa + kSlotV + ks * 2048, 8192, 1024),
+                                sdesc_sw128(sa + kOutTp + ks * 32, 16, 1024), id_u, ks > 0);
+                for (int ks = 0; ks < 8; ++ks) {
+                    const uint32_t oa = (ks >> 2) * 16384 + (ks & 3) * 32;
+                    const uint32_t oq = (ks >> 2) * 8192 + (ks & 3) * 32;
+                    mma_f16kind(tbase + kColSW, sdesc_sw128(sba + oa, 16, 1024),
+                                sdesc_sw128(sa + kOutW + ks * 2048, 8192, 1024), id_w, ks > 0);
+                    mma_f16kind(tbase + kColSQ + sl * 64, sdesc_sw128(sba + oa, 16, 1024),
+                                sdesc_sw128(sa + kSlotQ + oq, 16, 1024), id_q, ks > 0);
+                }
+                mma_commit(&s->mma1);
+            }
+            wait_bar(&s->mma1, c & 1, false, abort_flag, a.status);
+            tc_fence_after();
+
+            // V_new^T = U^T - S W^T -> VnT; V_new^T * e^{g_C - g} -> slot V region
+            {
+                const float *ekc = gs + 2 * kC;
+                float u[32], w[32];
+                for (int half = 0; half < 2; ++half) {
+                    tmem_ld32(lane_addr(tbase, quad, kColU + half * 32), u);
+                    tmem_ld32(lane_addr(tbase, quad, kColSW + half * 32), w);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) u[j] -= w[j];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) st_chunk(VnT, t, half * 4 + q, u + q * 8, &amax);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) u[j] *= ekc[half * 32 + j];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        st_chunk(slot + kSlotV, t, half * 4 + q, u + q * 8, &amax);
+                }
+            }
+            fence_async_smem();
+            tc_fence_before();
+            named_sync(1, 128);
+
+            // O_intra^T = V_new^T P^T;  S += (V_new e^{g_C-g})^T K
+            if (t == 0) {
+                tc_fence_after();
+                const uint32_t ido = idesc_f16_f32(128, 64, 0, 0);
+                const uint32_t ids = idesc_f16_f32(128, 128, 0, 1);
+                const uint32_t sa = smem_u32(slot), vn = smem_u32(VnT);
+                for (int ks = 0; ks < 4; ++ks) {
+                    mma_f16kind(tbase + kColO + sl * 64, sdesc_sw128(vn + ks * 32, 16, 1024),
+                                sdesc_sw128(sa + kOutP + ks * 32, 16, 1024), ido, ks > 0);
+                    mma_f16kind(tbase + kColS, sdesc_sw128(sa + kSlotV + ks * 32, 16, 1024),
+                                sdesc_sw128(sa + kSlotK + ks * 2048, 8192, 1024), ids, 1);
+                }
+                mma_commit(&s->mma2);
+                mma_commit(&s->out_full[sl]);
+            }
+            wait_bar(&s->mma2, c & 1, false, abort_flag, a.status);
+            tc_fence_after();
+            // slot consumed: hand it back to the producer, refill our tiles
+            if (t == 0) {
+                mbar_arrive_remote(r_slot_empty + sl * sizeof(uint64_t));
+                if (c + 2 < nchunks && !*abort_flag) issue_qkv(c + 2);
+            }
+        }
+        if (a.S_final && !*abort_flag) {
+            float *dst = a.S_final + (((size_t)n * H + h) * dv + v0 + t) * kDK;
+            for (int cb = 0; cb < 4; ++cb) {
+                float x[32];
+                tmem_ld32(lane_addr(tbase, quad, kColS + cb * 32), x);
                 tmem_ld_wait();
 #pragma unroll
-                for (int j = 0; j < 32; ++j) u[j] -= w[j];
-#pragma unroll
-                for (int q = 0; q < 4; ++q) st_chunk(VnT, tid, half * 4 + q, u + q * 8, &amax);
-#pragma unroll
-                for (int j = 0; j < 32; ++j) u[j] *= s->ekc[half * 32 + j];
-#pragma unroll
-                for (int q = 0; q < 4; ++q) st_chunk(VnTs, tid, half * 4 + q, u + q * 8, &amax);
+                for (int j = 0; j < 32; ++j) dst[cb * 32 + j] = x[j];
             }
         }
-        fence_async_smem();
-        tc_fence_before();
-        __syncthreads();
-
-        // -------- batch 4: O_intra^T = V_new^T P^T;  S += (V_new e^{gC-g})^T K
-        if (tid == 0) {
+    } else {
+        // ---------------- tile conversion and outputs (warps 4-7)
+        const int t = tid - 128;
+        __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(a.o);
+        auto convert = [&](int c) {
+            const int sl = c & 1;
+            uint8_t *slot = sm + sl * kSlotBytes;
+            const int nc = (int)min((long)kC, len - (long)c * kC);
+            wait_bar(&s->tma[sl], (c >> 1) & 1, false, abort_flag, a.status);
+            uint8_t *const tiles[6] = {slot + kSlotQ, slot + kSlotQ + 8192, slot + kSlotK,
+                                       slot + kSlotK + 8192, slot + kSlotV, slot + kSlotV + 8192};
+            convert_tiles<6>(tiles, nc, t, &amax);
+            fence_async_smem();
+            mbar_arrive(&s->conv[sl]);
+        };
+        auto output = [&](int c) {
+            const int sl = c & 1;
+            const int nc = (int)min((long)kC, len - (long)c * kC);
+            const long tok0 = start + (long)c * kC;
+            wait_bar(&s->egc_full[sl], (c >> 1) & 1, false, abort_flag, a.status);
+            wait_bar(&s->out_full[sl], (c >> 1) & 1, false, abort_flag, a.status);
             tc_fence_after();
-            const uint32_t ido = idesc_f16_f32(128, 64, 0, 0);
-            const uint32_t ids = idesc_f16_f32(128, 128, 0, 1);
-            const uint32_t kqa = smem_u32(kq);
-            for (int ks = 0; ks < 4; ++ks) {
-                mma_f16kind(tbase + kColO, sdesc_sw128(smem_u32(VnT) + ks * 32, 16, 1024),
-                         sdesc_sw128(smem_u32(Pm) + ks * 32, 16, 1024), ido, ks > 0);
-                mma_f16kind(tbase + kColS, sdesc_sw128(smem_u32(VnTs) + ks * 32, 16, 1024),
-                         sdesc_sw128(kqa + ks * 2048, 16384, 1024), ids, 1);
-            }
-            mma_commit(&s->bar_mma);
-        }
-        wait_or_abort(&s->bar_mma, mma_phase, s, a.status);
-        mma_phase ^= 1;
-        tc_fence_after();
-
-        // -------- o_i = e^{g_i} (S Q^T)[v][i] + O_intra^T[v][i]
-        {
-            __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(a.o);
-            const size_t col = (size_t)v0 + tid;
+            const size_t col = (size_t)v0 + t;
             float x[32], y[32];
             for (int half = 0; half < 2; ++half) {
-                tmem_ld32(lane_addr(tbase, warp, kColSQ + half * 32), x);
-                tmem_ld32(lane_addr(tbase, warp, kColO + half * 32), y);
+                tmem_ld32(lane_addr(tbase, quad, kColSQ + sl * 64 + half * 32), x);
+                tmem_ld32(lane_addr(tbase, quad, kColO + sl * 64 + half * 32), y);
                 tmem_ld_wait();
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
                     const int i = half * 32 + j;
                     if (i < nc)
                         o[((size_t)(tok0 + i) * H + h) * dv + col] =
-                            __float2bfloat16_rn(fmaf(s->eg[i], x[j], y[j]));
+                            __float2bfloat16_rn(fmaf(s->egc[sl][i], x[j], y[j]));
                 }
             }
+            tc_fence_before();
+            mbar_arrive(&s->out_done[sl]);
+        };
+        if (nchunks > 0) convert(0);
+        for (int c = 1; c < nchunks; ++c) {
+            convert(c);
+            output(c - 1);
         }
-        tc_fence_before();
-        __syncthreads();
-        if (s->abort_flag) break;
+        if (nchunks > 0) output(nchunks - 1);
     }
-
     if (amax > kF16Max) atomicOr(a.status, 0x4u);
+}
 
-    // -------- final state, or drain after an abort
-    if (!s->abort_flag) {
-        if (a.S_final) {
-            float *dst = a.S_final + (((size_t)n * H + h) * dv + v0 + tid) * kDK;
-            for (int cb = 0; cb < 4; ++cb) {
-                float x[32];
-                tmem_ld32(lane_addr(tbase, warp, kColS + cb * 32), x);
-                tmem_ld_wait();
-#pragma unroll
-                for (int j = 0; j < 32; ++j) dst[cb * 32 + j] = x[j];
-            }
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+gdn_tc_kernel(const GdnArgs a, const __grid_constant__ CUtensorMap tm_q,
+              const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const uint32_t rank = cluster_ctarank();  // 0 = producer, 1 = consumer
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int vt = blockIdx.x >> 1, h = blockIdx.y, n = blockIdx.z;
+    const int v0 = vt * kDVT;
+
+    long start = 0, len = 0;
+    if (a.cu_seqlens) {
+        const int s0 = a.cu_seqlens[n], e0 = a.cu_seqlens[n + 1];
+        if (s0 < 0 || e0 < s0 || e0 > a.T) {  // both CTAs see the same span and leave
+            if (tid == 0 && rank == 0) atomicOr(a.status, 0x1u);
+            return;
         }
-    } else if (tid == 0) {
-        // wait (bounded) for copies this CTA still has in flight
-        for (int cc = c; cc < kq_issued; ++cc) mbar_wait(&s->bar_kq[cc & 1], (cc >> 1) & 1, kWaitLimitNs);
-        for (int cc = c; cc < v_issued; ++cc) mbar_wait(&s->bar_v, cc & 1, kWaitLimitNs);
+        start = s0;
+        len = e0 - s0;
+    } else {
+        start = (long)n * a.T;
+        len = a.T;
     }
+    const int nchunks = (int)((len + kC - 1) / kC);
+
+    uint32_t *tmem_slot;
+    const uint32_t ncols = rank == 0 ? 256 : 512;
+    if (rank == 0) {
+        PSmall *s = reinterpret_cast<PSmall *>(sm + kPOffSmall);
+        tmem_slot = &s->tmem;
+        if (tid == 0) {
+            for (int i = 0; i < 2; ++i) {
+                mbar_init(&s->tma_in[i], 1);
+                mbar_init(&s->mma[i], 1);
+                mbar_init(&s->src_free[i], 1);
+                mbar_init(&s->slot_empty[i], 1);
+            }
+            s->abort_flag = 0;
+            fence_mbar_init();
+            prefetch_tensormap(&tm_q);
+            prefetch_tensormap(&tm_k);
+        }
+    } else {
+        CSmall *s = reinterpret_cast<CSmall *>(sm + kCOffSmall);
+        tmem_slot = &s->tmem;
+        if (tid == 0) {
+            for (int i = 0; i < 2; ++i) {
+                mbar_init(&s->full[i], 1);
+                mbar_init(&s->tma[i], 1);
+                mbar_init(&s->conv[i], 128);
+                mbar_init(&s->egc_full[i], kC);
+                mbar_init(&s->out_full[i], 1);
+                mbar_init(&s->out_done[i], 128);
+            }
+            mbar_init(&s->mma1, 1);
+            mbar_init(&s->mma2, 1);
+            s->abort_flag = 0;
+            fence_mbar_init();
+            prefetch_tensormap(&tm_q);
+            prefetch_tensormap(&tm_k);
+            prefetch_tensormap(&tm_v);
+        }
+    }
+    if (warp == 0) {
+        tmem_alloc(tmem_slot, ncols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    cluster_sync();  // the barriers of both CTAs exist before any remote arrive
+    tc_fence_after();
+    const uint32_t tbase = *tmem_slot;
+
+    if (rank == 0) producer(a, &tm_q, &tm_k, sm, tbase, start, len, nchunks, h);
+    else consumer(a, &tm_q, &tm_k, &tm_v, sm, tbase, start, len, nchunks, h, n, v0);
+
     tc_fence_before();
     __syncthreads();
     if (warp == 0) {
         tc_fence_after();
-        tmem_dealloc(tbase, 512);
+        tmem_dealloc(tbase, ncols);
     }
+    cluster_sync();  // no CTA leaves while its peer may still touch its memory
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encoder()
@@ -625,7 +774,7 @@ cudaError_t gdn_launch_tc(const GdnArgs &a, cudaStream_t s, int *launches)
     cudaError_t e = cudaFuncSetAttribute(gdn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          kSmemBytes);
     if (e != cudaSuccess) return e;
-    dim3 grid(a.dv / kDVT, a.H, a.N);
+    dim3 grid(2 * (a.dv / kDVT), a.H, a.N);
     gdn_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(a, mq, mk, mv);
     *launches = 1;
     return cudaGetLastError();
