@@ -141,15 +141,15 @@ __device__ __forceinline__ void chunk_bf16_to_f16(uint8_t *p, float *amax)
     *reinterpret_cast<uint4 *>(p) = make_uint4(w[0], w[1], w[2], w[3]);
 }
 
-// Convert `ntiles` 64-row x 128-byte tiles in place; rows at or past `nc` are
-// zeroed (they may belong to another sequence).
+// Convert NT 64-row x 128-byte tiles (tile i at base + i * 8192) in place;
+// rows at or past `nc` are zeroed (they may belong to another sequence).
 template <int NT>
-__device__ __forceinline__ void convert_tiles(uint8_t *const (&tiles)[NT], int nc, int t,
-                                              float *amax)
+__device__ __forceinline__ void convert_tiles(uint8_t *base, int nc, int t, float *amax)
 {
+#pragma unroll 4
     for (int idx = t; idx < NT * kC * 8; idx += 128) {
-        const int tile = idx / (kC * 8), r = (idx >> 3) & (kC - 1), cc = idx & 7;
-        uint8_t *p = tiles[tile] + sw128(r, cc);
+        const int r = (idx >> 3) & (kC - 1), cc = idx & 7;
+        uint8_t *p = base + (idx >> 9) * 8192 + sw128(r, cc);
         if (r < nc) chunk_bf16_to_f16(p, amax);
         else *reinterpret_cast<uint4 *>(p) = make_uint4(0, 0, 0, 0);
     }
@@ -226,6 +226,11 @@ __device__ __forceinline__ void producer(const GdnArgs &a, const CUtensorMap *tm
             }
         }
     };
+    // upper blocks of T that no phase writes but the merges read: zero once
+    for (int idx = t; idx < 2 * 16 * 16; idx += 128) {
+        const int b = idx >> 8, r = (idx >> 4) & 15, cc = idx & 15;
+        Ts[(32 * b + r) * kLdA + 32 * b + 16 + cc] = 0.f;
+    }
     if (p < nchunks && t == 0) issue_in(p);
     load_gates(p);
 
@@ -259,10 +264,7 @@ __device__ __forceinline__ void producer(const GdnArgs &a, const CUtensorMap *tm
 
         // q/k tiles -> fp16
         wait_bar(&s->tma_in[p], k & 1, false, abort_flag, a.status);
-        {
-            uint8_t *const tiles[4] = {in, in + 8192, in + 16384, in + 16384 + 8192};
-            convert_tiles<4>(tiles, nc, t, &amax);
-        }
+        convert_tiles<4>(in, nc, t, &amax);  // [K|Q] d_k half 0, [K|Q] half 1
         fence_async_smem();
         tc_fence_before();
         named_sync(bar_id, 128);
@@ -334,39 +336,76 @@ __device__ __forceinline__ void producer(const GdnArgs &a, const CUtensorMap *tm
             }
         }
         named_sync(bar_id, 128);
-        // (2) 16 -> 32: T[1,0] = -T11 (A10 T00) for block pairs (0,1) and (2,3)
-        for (int idx = t; idx < 512; idx += 128) {
-            const int pp = idx >> 8, r = (idx >> 4) & 15, cc = idx & 15;
+        // (2) 16 -> 32: T[1,0] = -T11 (A10 T00) for the block pairs (0,1), (2,3).
+        //     64 threads per pair, each a 1x4 block of the 16x16 result with
+        //     independent accumulators; the never-written upper blocks of T
+        //     are zero, so every loop has fixed bounds.
+        {
+            const int pp = t >> 6, r = (t & 63) >> 2, c4 = (t & 3) * 4;
             const int R = 16 * (2 * pp + 1), Cc = 32 * pp;
-            float acc = 0.f;
-            for (int m = cc; m < 16; ++m)
-                acc = fmaf(As[(R + r) * kLdA + Cc + m], Ts[(Cc + m) * kLdA + Cc + cc], acc);
-            Xs[pp * 16 * 17 + r * 17 + cc] = acc;
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int m = 0; m < 16; ++m) {
+                const float av = As[(R + r) * kLdA + Cc + m];
+                const float *tr = Ts + (Cc + m) * kLdA + Cc + c4;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) acc[e] = fmaf(av, tr[e], acc[e]);
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) Xs[pp * 16 * 17 + r * 17 + c4 + e] = acc[e];
+            named_sync(bar_id, 128);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[e] = 0.f;
+#pragma unroll
+            for (int m = 0; m < 16; ++m) {
+                const float tv = Ts[(R + r) * kLdA + R + m];
+                const float *xr = Xs + pp * 16 * 17 + m * 17 + c4;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) acc[e] = fmaf(tv, xr[e], acc[e]);
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) Ts[(R + r) * kLdA + Cc + c4 + e] = -acc[e];
         }
         named_sync(bar_id, 128);
-        for (int idx = t; idx < 512; idx += 128) {
-            const int pp = idx >> 8, r = (idx >> 4) & 15, cc = idx & 15;
-            const int R = 16 * (2 * pp + 1), Cc = 32 * pp;
-            float acc = 0.f;
-            for (int m = 0; m <= r; ++m)
-                acc = fmaf(Ts[(R + r) * kLdA + R + m], Xs[pp * 16 * 17 + m * 17 + cc], acc);
-            Ts[(R + r) * kLdA + Cc + cc] = -acc;
-        }
-        named_sync(bar_id, 128);
-        // (3) 32 -> 64: T[32:64, 0:32] = -T2 (A21 T1)
-        for (int idx = t; idx < 1024; idx += 128) {
-            const int r = idx >> 5, cc = idx & 31;
-            float acc = 0.f;
-            for (int m = cc; m < 32; ++m) acc = fmaf(As[(32 + r) * kLdA + m], Ts[m * kLdA + cc], acc);
-            Xs[r * 33 + cc] = acc;
-        }
-        named_sync(bar_id, 128);
-        for (int idx = t; idx < 1024; idx += 128) {
-            const int r = idx >> 5, cc = idx & 31;
-            float acc = 0.f;
-            for (int m = 0; m <= r; ++m)
-                acc = fmaf(Ts[(32 + r) * kLdA + 32 + m], Xs[m * 33 + cc], acc);
-            Ts[(32 + r) * kLdA + cc] = -acc;
+        // (3) 32 -> 64: T[32:64, 0:32] = -T2 (A21 T1); each thread a 2x4 block.
+        {
+            const int r2 = (t >> 3) * 2, c4 = (t & 7) * 4;
+            float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll 8
+            for (int m = 0; m < 32; ++m) {
+                const float a0 = As[(32 + r2) * kLdA + m], a1 = As[(33 + r2) * kLdA + m];
+                const float *tr = Ts + m * kLdA + c4;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float tv = tr[e];
+                    acc[0][e] = fmaf(a0, tv, acc[0][e]);
+                    acc[1][e] = fmaf(a1, tv, acc[1][e]);
+                }
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                Xs[r2 * 33 + c4 + e] = acc[0][e];
+                Xs[(r2 + 1) * 33 + c4 + e] = acc[1][e];
+            }
+            named_sync(bar_id, 128);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[0][e] = acc[1][e] = 0.f;
+#pragma unroll 8
+            for (int m = 0; m < 32; ++m) {
+                const float t0 = Ts[(32 + r2) * kLdA + 32 + m], t1 = Ts[(33 + r2) * kLdA + 32 + m];
+                const float *xr = Xs + m * 33 + c4;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float xv = xr[e];
+                    acc[0][e] = fmaf(t0, xv, acc[0][e]);
+                    acc[1][e] = fmaf(t1, xv, acc[1][e]);
+                }
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                Ts[(32 + r2) * kLdA + c4 + e] = -acc[0][e];
+                Ts[(33 + r2) * kLdA + c4 + e] = -acc[1][e];
+            }
         }
         named_sync(bar_id, 128);
         // T'' = T diag(beta e^g) (local, over A), T' = T diag(beta) (shipped)
@@ -493,17 +532,24 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
             // incoming state: fp16 copy for the MMAs, TMEM <- e^{g_C} S
             {
                 const float dC = __expf(gC);
-                for (int cb = 0; cb < 4; ++cb) {
-                    float x[32];
-                    tmem_ld32(lane_addr(tbase, quad, kColS + cb * 32), x);
+                for (int half = 0; half < 2; ++half) {  // one d_k half (64 columns) per step
+                    float x[32], y[32];
+                    const uint32_t col = kColS + half * 64;
+                    tmem_ld32(lane_addr(tbase, quad, col), x);
+                    tmem_ld32(lane_addr(tbase, quad, col + 32), y);
                     tmem_ld_wait();
-                    uint8_t *box = Sb + (cb >> 1) * 16384;
+                    uint8_t *box = Sb + half * 16384;
 #pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        st_chunk(box, t, (cb & 1) * 4 + q, x + q * 8, &amax);
+                    for (int q = 0; q < 4; ++q) st_chunk(box, t, q, x + q * 8, &amax);
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) x[j] *= dC;
-                    tmem_st32(lane_addr(tbase, quad, kColS + cb * 32), x);
+                    for (int q = 0; q < 4; ++q) st_chunk(box, t, 4 + q, y + q * 8, &amax);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        x[j] *= dC;
+                        y[j] *= dC;
+                    }
+                    tmem_st32(lane_addr(tbase, quad, col), x);
+                    tmem_st32(lane_addr(tbase, quad, col + 32), y);
                 }
                 tmem_st_wait();
             }
@@ -599,9 +645,7 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
             uint8_t *slot = sm + sl * kSlotBytes;
             const int nc = (int)min((long)kC, len - (long)c * kC);
             wait_bar(&s->tma[sl], (c >> 1) & 1, false, abort_flag, a.status);
-            uint8_t *const tiles[6] = {slot + kSlotQ, slot + kSlotQ + 8192, slot + kSlotK,
-                                       slot + kSlotK + 8192, slot + kSlotV, slot + kSlotV + 8192};
-            convert_tiles<6>(tiles, nc, t, &amax);
+            convert_tiles<6>(slot + kSlotQ, nc, t, &amax);  // Q, K, V are contiguous
             fence_async_smem();
             mbar_arrive(&s->conv[sl]);
         };
