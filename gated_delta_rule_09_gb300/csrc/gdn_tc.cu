@@ -109,8 +109,15 @@ __device__ __forceinline__ uint32_t pack_f16(float a, float b)
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
+__device__ __forceinline__ float max8_abs(const float *x)
+{
+    const float a = fmaxf(fabsf(x[0]), fabsf(x[1])), b = fmaxf(fabsf(x[2]), fabsf(x[3]));
+    const float c = fmaxf(fabsf(x[4]), fabsf(x[5])), d = fmaxf(fabsf(x[6]), fabsf(x[7]));
+    return fmaxf(fmaxf(a, b), fmaxf(c, d));
+}
+
 // 8 values -> fp16 into 16-byte chunk c of row r of a swizzled tile; their
-// magnitudes fold into *amax for the range check.
+// magnitude folds into *amax for the range check (one dependent op per call).
 __device__ __forceinline__ void st_chunk(uint8_t *tile, int r, int c, const float *x, float *amax)
 {
     uint4 u;
@@ -118,40 +125,50 @@ __device__ __forceinline__ void st_chunk(uint8_t *tile, int r, int c, const floa
     u.y = pack_f16(x[2], x[3]);
     u.z = pack_f16(x[4], x[5]);
     u.w = pack_f16(x[6], x[7]);
-    float m = *amax;
-#pragma unroll
-    for (int e = 0; e < 8; ++e) m = fmaxf(m, fabsf(x[e]));
-    *amax = m;
+    *amax = fmaxf(*amax, max8_abs(x));
     *reinterpret_cast<uint4 *>(tile + sw128(r, c)) = u;
 }
 
-// bf16 -> fp16 in place for one 16-byte chunk.
-__device__ __forceinline__ void chunk_bf16_to_f16(uint8_t *p, float *amax)
+// bf16 -> fp16 for the 8 values of one 16-byte chunk (returned), with their
+// largest magnitude folded into *amax.
+__device__ __forceinline__ uint4 chunk_bf16_to_f16(uint4 u, float *amax)
 {
-    uint4 u = *reinterpret_cast<const uint4 *>(p);
-    uint32_t w[4] = {u.x, u.y, u.z, u.w};
-    float m = *amax;
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+    float f[8];
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w[e]));
-        m = fmaxf(m, fmaxf(fabsf(f.x), fabsf(f.y)));
-        w[e] = pack_f16(f.x, f.y);
+        const float2 v = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w[e]));
+        f[2 * e] = v.x;
+        f[2 * e + 1] = v.y;
     }
-    *amax = m;
-    *reinterpret_cast<uint4 *>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+    *amax = fmaxf(*amax, max8_abs(f));
+    return make_uint4(pack_f16(f[0], f[1]), pack_f16(f[2], f[3]), pack_f16(f[4], f[5]),
+                      pack_f16(f[6], f[7]));
 }
 
-// Convert NT 64-row x 128-byte tiles (tile i at base + i * 8192) in place;
-// rows at or past `nc` are zeroed (they may belong to another sequence).
+// Convert NT 64-row x 128-byte tiles (tile i at base + i * 8192) in place,
+// four 16-byte chunks per thread at a time (loads first); rows at or past
+// `nc` are zeroed (they may belong to another sequence).
 template <int NT>
 __device__ __forceinline__ void convert_tiles(uint8_t *base, int nc, int t, float *amax)
 {
-#pragma unroll 4
-    for (int idx = t; idx < NT * kC * 8; idx += 128) {
-        const int r = (idx >> 3) & (kC - 1), cc = idx & 7;
-        uint8_t *p = base + (idx >> 9) * 8192 + sw128(r, cc);
-        if (r < nc) chunk_bf16_to_f16(p, amax);
-        else *reinterpret_cast<uint4 *>(p) = make_uint4(0, 0, 0, 0);
+    static_assert((NT * kC * 8) % 512 == 0, "whole rounds of 4 x 128 chunks");
+    for (int i0 = t; i0 < NT * kC * 8; i0 += 512) {
+        uint4 v[4];
+        uint8_t *ptr[4];
+        bool keep[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int idx = i0 + 128 * j;
+            const int r = (idx >> 3) & (kC - 1), cc = idx & 7;
+            ptr[j] = base + (idx >> 9) * 8192 + sw128(r, cc);
+            keep[j] = r < nc;
+            v[j] = *reinterpret_cast<const uint4 *>(ptr[j]);
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            *reinterpret_cast<uint4 *>(ptr[j]) =
+                keep[j] ? chunk_bf16_to_f16(v[j], amax) : make_uint4(0, 0, 0, 0);
     }
 }
 
