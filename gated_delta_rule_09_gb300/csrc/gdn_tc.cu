@@ -86,7 +86,7 @@ constexpr int kSmemBytes =
     (kCOffSmall > kPOffSmall ? kCOffSmall : kPOffSmall) + kSmallBytes + 1024;
 
 struct PSmall {
-    float scan[2][kC], beta[2][kC];
+    float scan[2][kC], beta[2][kC], colf[2][kC];
     uint64_t tma_in[2], mma[2], src_free[2], slot_empty[2];
     uint32_t tmem;
     int abort_flag;
@@ -277,6 +277,7 @@ __device__ __forceinline__ void producer(const GdnArgs &a, const CUtensorMap *tm
         if (t < kC) {
             gout[kC + t] = __expf(gout[t]);
             gout[2 * kC + t] = __expf(gC - gout[t]);
+            s->colf[p][t] = __expf(gout[31] - gout[t]);
         }
 
         // q/k tiles -> fp16
@@ -301,27 +302,46 @@ __device__ __forceinline__ void producer(const GdnArgs &a, const CUtensorMap *tm
         wait_bar(&s->mma[p], 0, false, abort_flag, a.status);
         tc_fence_after();
 
-        // A (fp32, rows 0-63) and P (fp16, rows 64-127)
+        // A (fp32, rows 0-63) and P (fp16, rows 64-127).  The decay factor
+        // e^{g_i - g_j} splits as e^{g_i - g_r} e^{g_r - g_j} around the middle
+        // of the chunk (g_r = g_31), so each entry costs two multiplies; if the
+        // chunk's total decay could push a factor out of fp32 range, every entry
+        // is exponentiated on its own instead.  Columns past the diagonal are 0.
         {
             const bool is_k = t < kC;
             const int i = is_k ? t : t - kC;
             const float gi = gout[i], bi = s->beta[p][i];
+            const float gr = gout[31];
+            const bool split = (gout[0] - gC) < 80.f;  // uniform across the CTA
+            const float rowf = (is_k ? bi : 1.f) * (split ? __expf(gi - gr) : 1.f);
+            const float *colf = s->colf[p];
             float x[32];
             for (int half = 0; half < 2; ++half) {
+                if (half == 1 && quad % 2 == 0) {  // rows 0-31 of A / P: all j >= 32 are zero
+                    if (is_k) {
+#pragma unroll
+                        for (int jj = 0; jj < 32; ++jj) As[i * kLdA + 32 + jj] = 0.f;
+                    } else {
+#pragma unroll
+                        for (int jj = 0; jj < 32; ++jj) x[jj] = 0.f;
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) st_chunk(out + kOutP, i, 4 + q, x + q * 8, &amax);
+                    }
+                    continue;
+                }
                 tmem_ld32(lane_addr(tcol, quad, half * 32), x);
                 tmem_ld_wait();
+#pragma unroll
+                for (int jj = 0; jj < 32; ++jj) {
+                    const int j = half * 32 + jj;
+                    const float d = split ? rowf * colf[j] : (is_k ? bi : 1.f) * __expf(gi - gout[j]);
+                    const bool keep = is_k ? (j < i) : (j <= i);
+                    x[jj] = keep ? x[jj] * d : 0.f;
+                }
                 if (is_k) {
 #pragma unroll
-                    for (int jj = 0; jj < 32; ++jj) {
-                        const int j = half * 32 + jj;
-                        As[i * kLdA + j] = (j < i) ? bi * x[jj] * __expf(gi - gout[j]) : 0.f;
-                    }
+                    for (int jj = 0; jj < 32; ++jj) As[i * kLdA + half * 32 + jj] = x[jj];
                 } else {
-#pragma unroll
-                    for (int jj = 0; jj < 32; ++jj) {
-                        const int j = half * 32 + jj;
-                        x[jj] = (j <= i) ? x[jj] * __expf(gi - gout[j]) : 0.f;
-                    }
 #pragma unroll
                     for (int q = 0; q < 4; ++q)
                         st_chunk(out + kOutP, i, half * 4 + q, x + q * 8, &amax);
