@@ -291,11 +291,11 @@ __device__ __forceinline__ void producer(const GdnArgs &a, const CUtensorMap *tm
         if (t == 0) {
             tc_fence_after();
             const uint32_t id = idesc_f16_f32(128, 64, 0, 0);
-            const uint32_t ia = smem_u32(in);
+            const uint64_t dkq = sdesc_sw128(smem_u32(in), 16, 1024);
+#pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
-                const uint32_t o = (ks >> 2) * 16384 + (ks & 3) * 32;
-                mma_f16kind(tcol, sdesc_sw128(ia + o, 16, 1024), sdesc_sw128(ia + o, 16, 1024), id,
-                            ks > 0);
+                const uint32_t o = ((ks >> 2) * 16384 + (ks & 3) * 32) >> 4;
+                mma_f16kind(tcol, dkq + o, dkq + o, id, ks > 0);
             }
             mma_commit(&s->mma[p]);
         }
@@ -469,10 +469,11 @@ __device__ __forceinline__ void producer(const GdnArgs &a, const CUtensorMap *tm
         if (t == 0) {
             tc_fence_after();
             const uint32_t idw = idesc_f16_f32(128, 64, 1, 0);
-            const uint32_t ia = smem_u32(in), tp = smem_u32(Tpp);
+            const uint64_t dk = sdesc_sw128(smem_u32(in), 16384, 1024);
+            const uint64_t dt = sdesc_sw128(smem_u32(Tpp), 16, 1024);
+#pragma unroll
             for (int ks = 0; ks < 4; ++ks)
-                mma_f16kind(tcol + 64, sdesc_sw128(ia + ks * 2048, 16384, 1024),
-                            sdesc_sw128(tp + ks * 32, 16, 1024), idw, ks > 0);
+                mma_f16kind(tcol + 64, dk + ks * (2048 >> 4), dt + ks * (32 >> 4), idw, ks > 0);
             mma_commit(&s->mma[p]);
         }
         wait_bar(&s->mma[p], 1, false, abort_flag, a.status);
@@ -600,17 +601,22 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
                 const uint32_t id_u = idesc_f16_f32(128, 64, 1, 0);
                 const uint32_t id_w = idesc_f16_f32(128, 64, 0, 1);
                 const uint32_t id_q = idesc_f16_f32(128, 64, 0, 0);
-                const uint32_t sa = smem_u32(slot), sba = smem_u32(Sb);
+                const uint32_t sa = smem_u32(slot);
+                const uint64_t dv = sdesc_sw128(sa + kSlotV, 8192, 1024);
+                const uint64_t dtp = sdesc_sw128(sa + kOutTp, 16, 1024);
+                const uint64_t ds = sdesc_sw128(smem_u32(Sb), 16, 1024);
+                const uint64_t dw = sdesc_sw128(sa + kOutW, 8192, 1024);
+                const uint64_t dq = sdesc_sw128(sa + kSlotQ, 16, 1024);
+                const uint32_t csq = tbase + kColSQ + sl * 64;
+#pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
-                    mma_f16kind(tbase + kColU, sdesc_sw128(sa + kSlotV + ks * 2048, 8192, 1024),
-                                sdesc_sw128(sa + kOutTp + ks * 32, 16, 1024), id_u, ks > 0);
+                    mma_f16kind(tbase + kColU, dv + ks * (2048 >> 4), dtp + ks * (32 >> 4), id_u, ks > 0);
+#pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
-                    const uint32_t oa = (ks >> 2) * 16384 + (ks & 3) * 32;
-                    const uint32_t oq = (ks >> 2) * 8192 + (ks & 3) * 32;
-                    mma_f16kind(tbase + kColSW, sdesc_sw128(sba + oa, 16, 1024),
-                                sdesc_sw128(sa + kOutW + ks * 2048, 8192, 1024), id_w, ks > 0);
-                    mma_f16kind(tbase + kColSQ + sl * 64, sdesc_sw128(sba + oa, 16, 1024),
-                                sdesc_sw128(sa + kSlotQ + oq, 16, 1024), id_q, ks > 0);
+                    const uint32_t oa = ((ks >> 2) * 16384 + (ks & 3) * 32) >> 4;
+                    const uint32_t oq = ((ks >> 2) * 8192 + (ks & 3) * 32) >> 4;
+                    mma_f16kind(tbase + kColSW, ds + oa, dw + ks * (2048 >> 4), id_w, ks > 0);
+                    mma_f16kind(csq, ds + oa, dq + oq, id_q, ks > 0);
                 }
                 mma_commit(&s->mma1);
             }
@@ -645,12 +651,16 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
                 tc_fence_after();
                 const uint32_t ido = idesc_f16_f32(128, 64, 0, 0);
                 const uint32_t ids = idesc_f16_f32(128, 128, 0, 1);
-                const uint32_t sa = smem_u32(slot), vn = smem_u32(VnT);
+                const uint32_t sa = smem_u32(slot);
+                const uint64_t dvn = sdesc_sw128(smem_u32(VnT), 16, 1024);
+                const uint64_t dp = sdesc_sw128(sa + kOutP, 16, 1024);
+                const uint64_t dvs = sdesc_sw128(sa + kSlotV, 16, 1024);
+                const uint64_t dk = sdesc_sw128(sa + kSlotK, 8192, 1024);
+                const uint32_t co = tbase + kColO + sl * 64;
+#pragma unroll
                 for (int ks = 0; ks < 4; ++ks) {
-                    mma_f16kind(tbase + kColO + sl * 64, sdesc_sw128(vn + ks * 32, 16, 1024),
-                                sdesc_sw128(sa + kOutP + ks * 32, 16, 1024), ido, ks > 0);
-                    mma_f16kind(tbase + kColS, sdesc_sw128(sa + kSlotV + ks * 32, 16, 1024),
-                                sdesc_sw128(sa + kSlotK + ks * 2048, 8192, 1024), ids, 1);
+                    mma_f16kind(co, dvn + ks * (32 >> 4), dp + ks * (32 >> 4), ido, ks > 0);
+                    mma_f16kind(tbase + kColS, dvs + ks * (32 >> 4), dk + ks * (2048 >> 4), ids, 1);
                 }
                 mma_commit(&s->mma2);
                 mma_commit(&s->out_full[sl]);
