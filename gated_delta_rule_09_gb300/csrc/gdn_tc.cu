@@ -153,6 +153,7 @@ template <int NT>
 __device__ __forceinline__ void convert_tiles(uint8_t *base, int nc, int t, float *amax)
 {
     static_assert((NT * kC * 8) % 512 == 0, "whole rounds of 4 x 128 chunks");
+#pragma unroll 1
     for (int i0 = t; i0 < NT * kC * 8; i0 += 512) {
         uint4 v[4];
         uint8_t *ptr[4];
@@ -177,17 +178,17 @@ __device__ __forceinline__ uint32_t lane_addr(uint32_t tbase, int quad, uint32_t
     return tbase + (static_cast<uint32_t>(quad * 32) << 16) + col;
 }
 
-// Bounded wait; once this CTA has given up on one wait, every later wait
-// returns immediately so the kernel winds down.
-__device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, bool cluster_scope,
-                                         volatile int *abort_flag, unsigned int *status)
+// Bounded waits, kept out of line (about twenty call sites): once this CTA has
+// given up on one wait, every later wait returns immediately so the kernel
+// winds down.
+__device__ __noinline__ bool wait_cta(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                      unsigned int *status)
 {
     if (*abort_flag) return false;
-    if (cluster_scope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (;;) {
-        if (cluster_scope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity))
-            return true;
+        if (mbar_try_wait(bar, parity)) return true;
         if (*abort_flag) return false;
         if (globaltimer_ns() - t0 > kWaitLimitNs) {
             *abort_flag = 1;
@@ -195,6 +196,30 @@ __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, bool cl
             return false;
         }
     }
+}
+
+__device__ __noinline__ bool wait_cluster(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                          unsigned int *status)
+{
+    if (*abort_flag) return false;
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+        if (mbar_try_wait_cluster(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            *abort_flag = 1;
+            atomicOr(status, 0x2u);
+            return false;
+        }
+    }
+}
+
+__device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, bool cluster_scope,
+                                         volatile int *abort_flag, unsigned int *status)
+{
+    return cluster_scope ? wait_cluster(bar, parity, abort_flag, status)
+                         : wait_cta(bar, parity, abort_flag, status);
 }
 
 // ======================================================================
@@ -316,6 +341,7 @@ __device__ __forceinline__ void producer(const GdnArgs &a, const CUtensorMap *tm
             const float rowf = (is_k ? bi : 1.f) * (split ? __expf(gi - gr) : 1.f);
             const float *colf = s->colf[p];
             float x[32];
+            #pragma unroll 1
             for (int half = 0; half < 2; ++half) {
                 if (half == 1 && quad % 2 == 0) {  // rows 0-31 of A / P: all j >= 32 are zero
                     if (is_k) {
@@ -331,12 +357,27 @@ __device__ __forceinline__ void producer(const GdnArgs &a, const CUtensorMap *tm
                 }
                 tmem_ld32(lane_addr(tcol, quad, half * 32), x);
                 tmem_ld_wait();
+                if (split) {
 #pragma unroll
-                for (int jj = 0; jj < 32; ++jj) {
-                    const int j = half * 32 + jj;
-                    const float d = split ? rowf * colf[j] : (is_k ? bi : 1.f) * __expf(gi - gout[j]);
-                    const bool keep = is_k ? (j < i) : (j <= i);
-                    x[jj] = keep ? x[jj] * d : 0.f;
+                    for (int jj = 0; jj < 32; ++jj) {
+                        const int j = half * 32 + jj;
+                        const bool keep = is_k ? (j < i) : (j <= i);
+                        x[jj] = keep ? x[jj] * (rowf * colf[j]) : 0.f;
+                    }
+                } else {  // extreme in-chunk decay: exponentiate each entry
+                    const float base = is_k ? bi : 1.f;
+#pragma unroll 1
+                    for (int jj = 0; jj < 32; ++jj) {
+                        const int j = half * 32 + jj;
+                        const bool keep = is_k ? (j < i) : (j <= i);
+                        const float d = base * __expf(gi - gout[j]);
+                        float v = 0.f;
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) v = (e == jj) ? x[e] : v;
+                        v = keep ? v * d : 0.f;
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) x[e] = (e == jj) ? v : x[e];
+                    }
                 }
                 if (is_k) {
 #pragma unroll
@@ -451,6 +492,7 @@ __device__ __forceinline__ void producer(const GdnArgs &a, const CUtensorMap *tm
             const int j = first ? t : t - kC;
             uint8_t *dst = first ? Tpp : out + kOutTp;
             float x[8];
+#pragma unroll 1
             for (int q = 0; q < 8; ++q) {
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
@@ -484,6 +526,7 @@ __device__ __forceinline__ void producer(const GdnArgs &a, const CUtensorMap *tm
         // W^T rows (lane = d) -> MN-major B operand of S W^T
         {
             float x[32];
+            #pragma unroll 1
             for (int half = 0; half < 2; ++half) {
                 tmem_ld32(lane_addr(tcol + 64, quad, half * 32), x);
                 tmem_ld_wait();
@@ -570,6 +613,7 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
             // incoming state: fp16 copy for the MMAs, TMEM <- e^{g_C} S
             {
                 const float dC = __expf(gC);
+                #pragma unroll 1
                 for (int half = 0; half < 2; ++half) {  // one d_k half (64 columns) per step
                     float x[32], y[32];
                     const uint32_t col = kColS + half * 64;
@@ -627,6 +671,7 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
             {
                 const float *ekc = gs + 2 * kC;
                 float u[32], w[32];
+                #pragma unroll 1
                 for (int half = 0; half < 2; ++half) {
                     tmem_ld32(lane_addr(tbase, quad, kColU + half * 32), u);
                     tmem_ld32(lane_addr(tbase, quad, kColSW + half * 32), w);
@@ -705,6 +750,7 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
             tc_fence_after();
             const size_t col = (size_t)v0 + t;
             float x[32], y[32];
+            #pragma unroll 1
             for (int half = 0; half < 2; ++half) {
                 tmem_ld32(lane_addr(tbase, quad, kColSQ + sl * 64 + half * 32), x);
                 tmem_ld32(lane_addr(tbase, quad, kColO + sl * 64 + half * 32), y);
