@@ -60,25 +60,26 @@ constexpr float kF16Max = 65504.f;
 constexpr int kLdA = 65;     // padded fp32 row stride of A / T
 
 // ---- a ring slot: what the producer ships, then the consumer's own tiles
-constexpr int kOutW = 0;           // W^T rows d (MN-major B operand), fp16
-constexpr int kOutP = 16384;       // P rows i (K-major), fp16
-constexpr int kOutTp = 24576;      // T' rows j (K-major), fp16
-constexpr int kOutG = 32768;       // g[64], e^g[64], e^{g_C-g}[64] fp32
-constexpr int kOutBytes = 33792;   // shipped per chunk
+constexpr int kOutP = 0;           // P rows i (K-major), fp16
+constexpr int kOutTp = 8192;       // T' = T diag(beta) rows j (K-major), fp16
+constexpr int kOutTpp = 16384;     // T'' = T diag(beta e^g) rows j (K-major), fp16
+constexpr int kOutG = 24576;       // g[64], e^g[64], e^{g_C-g}[64] fp32
+constexpr int kOutBytes = 25600;   // shipped per chunk
 constexpr int kSlotQ = kOutBytes;          // Q, 2 d_k halves x 64 rows x 128 B
 constexpr int kSlotK = kSlotQ + 16384;     // K, same
 constexpr int kSlotV = kSlotK + 16384;     // V, 2 d_v halves (later V_new * e^{g_C-g})
 constexpr int kSlotBytes = kSlotV + 16384;
 
 // ---- producer shared memory (per pipeline p = 0, 1)
-constexpr int kPIn = 32768;                        // [K | Q] per d_k half
+constexpr int kPIn = 32768;                        // [K | Q] per d_k half, bf16
 constexpr int kPAT = 38912;                        // fp32 A[64][65] | T[64][65] | X[32][33]
 constexpr int kPOffIn = 0;
 constexpr int kPOffOut = kPOffIn + 2 * kPIn;
 constexpr int kPOffAT = kPOffOut + 2 * kOutBytes;
 constexpr int kPOffSmall = kPOffAT + 2 * kPAT;
 // ---- consumer shared memory
-constexpr int kCOffSb = 2 * kSlotBytes;            // S as fp16, 2 d_k halves x 128 rows
+constexpr int kCOffW = 2 * kSlotBytes;             // W^T rows d (MN-major B operand), fp16
+constexpr int kCOffSb = kCOffW + 16384;            // S as fp16, 2 d_k halves x 128 rows
 constexpr int kCOffVnT = kCOffSb + 32768;          // V_new^T rows v (K-major), fp16
 constexpr int kCOffSmall = kCOffVnT + 16384;
 constexpr int kSmallBytes = 2048;
@@ -93,14 +94,15 @@ struct PSmall {
 };
 struct CSmall {
     float egc[2][kC];
-    uint64_t full[2], tma[2], conv[2], egc_full[2], mma1, mma2, out_full[2], out_done[2];
+    uint64_t full[2], tma[2], conv[2], egc_full[2], w_mma, w_ready, mma1, mma2, out_full[2],
+        out_done[2];
     uint32_t tmem;
     int abort_flag;
 };
 static_assert(sizeof(PSmall) <= kSmallBytes && sizeof(CSmall) <= kSmallBytes, "small blocks");
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 
-// consumer TMEM columns (512): S W^T | U^T | S Q^T x2 | O_intra^T x2 | S
+// consumer TMEM columns (512): W^T then S W^T | U^T | S Q^T x2 | O_intra^T x2 | S
 constexpr uint32_t kColSW = 0, kColU = 64, kColSQ = 128, kColO = 256, kColS = 384;
 
 __device__ __forceinline__ uint32_t pack_f16(float a, float b)
@@ -239,9 +241,8 @@ __device__ __forceinline__ void producer(const GdnArgs &a, const CUtensorMap *tm
     float *As = reinterpret_cast<float *>(sm + kPOffAT + p * kPAT);
     float *Ts = As + kC * kLdA;
     float *Xs = Ts + kC * kLdA;
-    uint8_t *Tpp = reinterpret_cast<uint8_t *>(As);  // written once the inverse is done
     float *gout = reinterpret_cast<float *>(out + kOutG);
-    const uint32_t tcol = tbase + p * 128;           // [K;Q]K^T at +0, W^T at +64
+    const uint32_t tcol = tbase + p * 64;            // [K;Q] K^T
     const uint32_t r_full =
         mapa_shared(sm + kCOffSmall + offsetof(CSmall, full) + p * sizeof(uint64_t), 1);
     const uint32_t r_slot = mapa_shared(sm + p * kSlotBytes, 1);
@@ -305,17 +306,24 @@ __device__ __forceinline__ void producer(const GdnArgs &a, const CUtensorMap *tm
             s->colf[p][t] = __expf(gout[31] - gout[t]);
         }
 
-        // q/k tiles -> fp16
+        // q/k tiles (bf16: K K^T and Q K^T are exact products); rows past the
+        // sequence are zeroed (they may hold another sequence)
         wait_bar(&s->tma_in[p], k & 1, false, abort_flag, a.status);
-        convert_tiles<4>(in, nc, t, &amax);  // [K|Q] d_k half 0, [K|Q] half 1
-        fence_async_smem();
+        if (nc < kC) {
+            for (int idx = t; idx < 4 * (kC - nc) * 8; idx += 128) {
+                const int tile = idx / ((kC - nc) * 8), rem = idx % ((kC - nc) * 8);
+                *reinterpret_cast<uint4 *>(in + tile * 8192 + sw128(nc + (rem >> 3), rem & 7)) =
+                    make_uint4(0, 0, 0, 0);
+            }
+            fence_async_smem();
+        }
         tc_fence_before();
         named_sync(bar_id, 128);
 
         // [K;Q] K^T: lanes 0-63 K K^T, lanes 64-127 Q K^T
         if (t == 0) {
             tc_fence_after();
-            const uint32_t id = idesc_f16_f32(128, 64, 0, 0);
+            const uint32_t id = idesc_bf16_f32(128, 64, 0, 0);
             const uint64_t dkq = sdesc_sw128(smem_u32(in), 16, 1024);
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
@@ -324,8 +332,10 @@ __device__ __forceinline__ void producer(const GdnArgs &a, const CUtensorMap *tm
             }
             mma_commit(&s->mma[p]);
         }
-        wait_bar(&s->mma[p], 0, false, abort_flag, a.status);
+        wait_bar(&s->mma[p], k & 1, false, abort_flag, a.status);
         tc_fence_after();
+        // the q/k buffer is free: fetch the pipeline's next chunk
+        if (t == 0 && c + 2 < nchunks && !*abort_flag) issue_in(c + 2);
 
         // A (fp32, rows 0-63) and P (fp16, rows 64-127).  The decay factor
         // e^{g_i - g_j} splits as e^{g_i - g_r} e^{g_r - g_j} around the middle
@@ -486,11 +496,11 @@ __device__ __forceinline__ void producer(const GdnArgs &a, const CUtensorMap *tm
             }
         }
         named_sync(bar_id, 128);
-        // T'' = T diag(beta e^g) (local, over A), T' = T diag(beta) (shipped)
+        // T'' = T diag(beta e^g) and T' = T diag(beta), both shipped
         {
             const bool first = t < kC;
             const int j = first ? t : t - kC;
-            uint8_t *dst = first ? Tpp : out + kOutTp;
+            uint8_t *dst = first ? out + kOutTpp : out + kOutTp;
             float x[8];
 #pragma unroll 1
             for (int q = 0; q < 8; ++q) {
@@ -504,42 +514,9 @@ __device__ __forceinline__ void producer(const GdnArgs &a, const CUtensorMap *tm
             }
         }
         fence_async_smem();
-        tc_fence_before();
         named_sync(bar_id, 128);
 
-        // W^T = K^T T''^T  (A = K read MN-major over the two d_k halves)
-        if (t == 0) {
-            tc_fence_after();
-            const uint32_t idw = idesc_f16_f32(128, 64, 1, 0);
-            const uint64_t dk = sdesc_sw128(smem_u32(in), 16384, 1024);
-            const uint64_t dt = sdesc_sw128(smem_u32(Tpp), 16, 1024);
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-                mma_f16kind(tcol + 64, dk + ks * (2048 >> 4), dt + ks * (32 >> 4), idw, ks > 0);
-            mma_commit(&s->mma[p]);
-        }
-        wait_bar(&s->mma[p], 1, false, abort_flag, a.status);
-        tc_fence_after();
-        // the q/k buffer is free: fetch the pipeline's next chunk
-        if (t == 0 && c + 2 < nchunks && !*abort_flag) issue_in(c + 2);
-
-        // W^T rows (lane = d) -> MN-major B operand of S W^T
-        {
-            float x[32];
-            #pragma unroll 1
-            for (int half = 0; half < 2; ++half) {
-                tmem_ld32(lane_addr(tcol + 64, quad, half * 32), x);
-                tmem_ld_wait();
-#pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    st_chunk(out + kOutW, t, half * 4 + q, x + q * 8, &amax);
-            }
-        }
-        fence_async_smem();
-        tc_fence_before();
-        named_sync(bar_id, 128);
-
-        // ship W, P, T' and the decay vectors once the consumer's slot is free
+        // ship P, T', T'' and the decay vectors once the consumer's slot is free
         if (t == 0) {
             if (wait_bar(&s->slot_empty[p], (k + 1) & 1, true, abort_flag, a.status)) {
                 mbar_arrive_expect_tx_remote(r_full, kOutBytes);
@@ -563,7 +540,7 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
     const int tid = threadIdx.x, warp = tid >> 5;
     const int quad = warp & 3;
     const int H = a.H, dv = a.dv;
-    uint8_t *Sb = sm + kCOffSb, *VnT = sm + kCOffVnT;
+    uint8_t *Sb = sm + kCOffSb, *VnT = sm + kCOffVnT, *Wt = sm + kCOffW;
     const uint32_t r_src_free = mapa_shared(sm + kPOffSmall + offsetof(PSmall, src_free), 0);
     const uint32_t r_slot_empty = mapa_shared(sm + kPOffSmall + offsetof(PSmall, slot_empty), 0);
     float amax = 0.f;
@@ -603,7 +580,25 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
             wait_bar(&s->full[sl], kk & 1, true, abort_flag, a.status);
             wait_bar(&s->conv[sl], kk & 1, false, abort_flag, a.status);
             wait_bar(&s->out_done[sl], (kk + 1) & 1, false, abort_flag, a.status);
-            if (t == 0) mbar_arrive_remote(r_src_free + sl * sizeof(uint64_t));
+            if (t == 0) {
+                mbar_arrive_remote(r_src_free + sl * sizeof(uint64_t));
+                // state-independent products of this chunk, while the state copy runs:
+                // W^T = K^T T''^T into the S W^T columns (read out by warps 4-7),
+                // U^T = V^T T'^T
+                tc_fence_after();
+                const uint32_t id_w = idesc_f16_f32(128, 64, 1, 0);
+                const uint32_t sa = smem_u32(slot);
+                const uint64_t dk = sdesc_sw128(sa + kSlotK, 8192, 1024);
+                const uint64_t dtpp = sdesc_sw128(sa + kOutTpp, 16, 1024);
+                const uint64_t dv = sdesc_sw128(sa + kSlotV, 8192, 1024);
+                const uint64_t dtp = sdesc_sw128(sa + kOutTp, 16, 1024);
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks) {
+                    mma_f16kind(tbase + kColSW, dk + ks * (2048 >> 4), dtpp + ks * (32 >> 4), id_w, ks > 0);
+                    mma_f16kind(tbase + kColU, dv + ks * (2048 >> 4), dtp + ks * (32 >> 4), id_w, ks > 0);
+                }
+                mma_commit(&s->w_mma);
+            }
             if (t < kC) {
                 s->egc[sl][t] = gs[kC + t];
                 mbar_arrive(&s->egc_full[sl]);
@@ -639,22 +634,17 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
             tc_fence_before();
             named_sync(1, 128);
 
-            // U^T = V^T T'^T;  S W^T;  S Q^T
+            // S W^T;  S Q^T  (W^T rows written by warps 4-7)
+            wait_bar(&s->w_ready, c & 1, false, abort_flag, a.status);
             if (t == 0) {
                 tc_fence_after();
-                const uint32_t id_u = idesc_f16_f32(128, 64, 1, 0);
                 const uint32_t id_w = idesc_f16_f32(128, 64, 0, 1);
                 const uint32_t id_q = idesc_f16_f32(128, 64, 0, 0);
                 const uint32_t sa = smem_u32(slot);
-                const uint64_t dv = sdesc_sw128(sa + kSlotV, 8192, 1024);
-                const uint64_t dtp = sdesc_sw128(sa + kOutTp, 16, 1024);
                 const uint64_t ds = sdesc_sw128(smem_u32(Sb), 16, 1024);
-                const uint64_t dw = sdesc_sw128(sa + kOutW, 8192, 1024);
+                const uint64_t dw = sdesc_sw128(smem_u32(Wt), 8192, 1024);
                 const uint64_t dq = sdesc_sw128(sa + kSlotQ, 16, 1024);
                 const uint32_t csq = tbase + kColSQ + sl * 64;
-#pragma unroll
-                for (int ks = 0; ks < 4; ++ks)
-                    mma_f16kind(tbase + kColU, dv + ks * (2048 >> 4), dtp + ks * (32 >> 4), id_u, ks > 0);
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
                     const uint32_t oa = ((ks >> 2) * 16384 + (ks & 3) * 32) >> 4;
@@ -766,10 +756,29 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
             tc_fence_before();
             mbar_arrive(&s->out_done[sl]);
         };
-        if (nchunks > 0) convert(0);
+        auto w_epilogue = [&](int c) {
+            wait_bar(&s->w_mma, c & 1, false, abort_flag, a.status);
+            tc_fence_after();
+            float x[32];
+#pragma unroll 1
+            for (int half = 0; half < 2; ++half) {
+                tmem_ld32(lane_addr(tbase, quad, kColSW + half * 32), x);
+                tmem_ld_wait();
+#pragma unroll
+                for (int q = 0; q < 4; ++q) st_chunk(Wt, t, half * 4 + q, x + q * 8, &amax);
+            }
+            fence_async_smem();
+            tc_fence_before();
+            mbar_arrive(&s->w_ready);
+        };
+        if (nchunks > 0) {
+            convert(0);
+            w_epilogue(0);
+        }
         for (int c = 1; c < nchunks; ++c) {
             convert(c);
             output(c - 1);
+            w_epilogue(c);
         }
         if (nchunks > 0) output(nchunks - 1);
     }
@@ -804,7 +813,7 @@ gdn_tc_kernel(const GdnArgs a, const __grid_constant__ CUtensorMap tm_q,
     const int nchunks = (int)((len + kC - 1) / kC);
 
     uint32_t *tmem_slot;
-    const uint32_t ncols = rank == 0 ? 256 : 512;
+    const uint32_t ncols = rank == 0 ? 128 : 512;
     if (rank == 0) {
         PSmall *s = reinterpret_cast<PSmall *>(sm + kPOffSmall);
         tmem_slot = &s->tmem;
@@ -832,6 +841,8 @@ gdn_tc_kernel(const GdnArgs a, const __grid_constant__ CUtensorMap tm_q,
                 mbar_init(&s->out_full[i], 1);
                 mbar_init(&s->out_done[i], 128);
             }
+            mbar_init(&s->w_mma, 1);
+            mbar_init(&s->w_ready, 128);
             mbar_init(&s->mma1, 1);
             mbar_init(&s->mma2, 1);
             s->abort_flag = 0;
