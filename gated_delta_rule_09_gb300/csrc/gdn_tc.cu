@@ -573,6 +573,33 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
             }
             tmem_st_wait();
         }
+        // state-independent products of chunk c, issued one chunk ahead so
+        // warps 4-7 read W^T out while the state chain runs: W^T = K^T T''^T
+        // into the S W^T columns, U^T = V^T T'^T.  Needs chunk c's slot
+        // (producer data and converted tiles).
+        auto issue_wu = [&](int c) {
+            uint8_t *slot = sm + (c & 1) * kSlotBytes;
+            const uint32_t id_w = idesc_f16_f32(128, 64, 1, 0);
+            const uint32_t sa = smem_u32(slot);
+            const uint64_t dk = sdesc_sw128(sa + kSlotK, 8192, 1024);
+            const uint64_t dtpp = sdesc_sw128(sa + kOutTpp, 16, 1024);
+            const uint64_t dv = sdesc_sw128(sa + kSlotV, 8192, 1024);
+            const uint64_t dtp = sdesc_sw128(sa + kOutTp, 16, 1024);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {
+                mma_f16kind(tbase + kColSW, dk + ks * (2048 >> 4), dtpp + ks * (32 >> 4), id_w, ks > 0);
+                mma_f16kind(tbase + kColU, dv + ks * (2048 >> 4), dtp + ks * (32 >> 4), id_w, ks > 0);
+            }
+            mma_commit(&s->w_mma);
+        };
+        if (nchunks > 0) {
+            wait_bar(&s->full[0], 0, true, abort_flag, a.status);
+            wait_bar(&s->conv[0], 0, false, abort_flag, a.status);
+            if (t == 0) {
+                tc_fence_after();
+                issue_wu(0);
+            }
+        }
         for (int c = 0; c < nchunks; ++c) {
             const int sl = c & 1, kk = c >> 1;
             uint8_t *slot = sm + sl * kSlotBytes;
@@ -580,25 +607,7 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
             wait_bar(&s->full[sl], kk & 1, true, abort_flag, a.status);
             wait_bar(&s->conv[sl], kk & 1, false, abort_flag, a.status);
             wait_bar(&s->out_done[sl], (kk + 1) & 1, false, abort_flag, a.status);
-            if (t == 0) {
-                mbar_arrive_remote(r_src_free + sl * sizeof(uint64_t));
-                // state-independent products of this chunk, while the state copy runs:
-                // W^T = K^T T''^T into the S W^T columns (read out by warps 4-7),
-                // U^T = V^T T'^T
-                tc_fence_after();
-                const uint32_t id_w = idesc_f16_f32(128, 64, 1, 0);
-                const uint32_t sa = smem_u32(slot);
-                const uint64_t dk = sdesc_sw128(sa + kSlotK, 8192, 1024);
-                const uint64_t dtpp = sdesc_sw128(sa + kOutTpp, 16, 1024);
-                const uint64_t dv = sdesc_sw128(sa + kSlotV, 8192, 1024);
-                const uint64_t dtp = sdesc_sw128(sa + kOutTp, 16, 1024);
-#pragma unroll
-                for (int ks = 0; ks < 4; ++ks) {
-                    mma_f16kind(tbase + kColSW, dk + ks * (2048 >> 4), dtpp + ks * (32 >> 4), id_w, ks > 0);
-                    mma_f16kind(tbase + kColU, dv + ks * (2048 >> 4), dtp + ks * (32 >> 4), id_w, ks > 0);
-                }
-                mma_commit(&s->w_mma);
-            }
+            if (t == 0) mbar_arrive_remote(r_src_free + sl * sizeof(uint64_t));
             if (t < kC) {
                 s->egc[sl][t] = gs[kC + t];
                 mbar_arrive(&s->egc_full[sl]);
@@ -700,6 +709,11 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
                 mma_commit(&s->mma2);
                 mma_commit(&s->out_full[sl]);
             }
+            if (c + 1 < nchunks) {  // next chunk's W^T, U^T (their columns are free now)
+                wait_bar(&s->full[sl ^ 1], ((c + 1) >> 1) & 1, true, abort_flag, a.status);
+                wait_bar(&s->conv[sl ^ 1], ((c + 1) >> 1) & 1, false, abort_flag, a.status);
+                if (t == 0) issue_wu(c + 1);
+            }
             wait_bar(&s->mma2, c & 1, false, abort_flag, a.status);
             tc_fence_after();
             // slot consumed: hand it back to the producer, refill our tiles
@@ -777,8 +791,8 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
         }
         for (int c = 1; c < nchunks; ++c) {
             convert(c);
-            output(c - 1);
             w_epilogue(c);
+            output(c - 1);
         }
         if (nchunks > 0) output(nchunks - 1);
     }
