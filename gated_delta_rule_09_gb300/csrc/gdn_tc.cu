@@ -64,15 +64,14 @@ constexpr int kOutP = 0;           // P rows i (K-major), fp16
 constexpr int kOutTp = 8192;       // T' = T diag(beta) rows j (K-major), fp16
 constexpr int kOutTpp = 16384;     // T'' = T diag(beta e^g) rows j (K-major), fp16
 constexpr int kOutG = 24576;       // g[64], e^g[64], e^{g_C-g}[64] fp32
-constexpr int kOutBytes = 25600;   // shipped per chunk
-constexpr int kSlotQ = kOutBytes;          // Q, 2 d_k halves x 64 rows x 128 B
-constexpr int kSlotK = kSlotQ + 16384;     // K, same
-constexpr int kSlotV = kSlotK + 16384;     // V, 2 d_v halves (later V_new * e^{g_C-g})
+constexpr int kOutKQ = 25600;      // fp16 [K rows | Q rows] per d_k half (2 x 16 KB)
+constexpr int kOutBytes = 58368;   // shipped per chunk
+constexpr int kSlotV = kOutBytes;          // V, 2 d_v halves (later V_new * e^{g_C-g})
 constexpr int kSlotBytes = kSlotV + 16384;
 
 // ---- producer shared memory (per pipeline p = 0, 1)
-constexpr int kPIn = 32768;                        // [K | Q] per d_k half, bf16
-constexpr int kPAT = 38912;                        // fp32 A[64][65] | T[64][65] | X[32][33]
+constexpr int kPIn = 32768;                        // [K | Q] per d_k half, bf16 (TMA)
+constexpr int kPAT = 21504;                        // fp32 A then T in place [64][65] | X[32][33]
 constexpr int kPOffIn = 0;
 constexpr int kPOffOut = kPOffIn + 2 * kPIn;
 constexpr int kPOffAT = kPOffOut + 2 * kOutBytes;
@@ -175,6 +174,23 @@ __device__ __forceinline__ void convert_tiles(uint8_t *base, int nc, int t, floa
     }
 }
 
+// bf16 -> fp16 copy of NT 64-row x 128-byte tiles from `src` to `dst` (same
+// swizzled positions), four 16-byte chunks per thread at a time.
+template <int NT>
+__device__ __forceinline__ void convert_copy_tiles(const uint8_t *src, uint8_t *dst, int t,
+                                                   float *amax)
+{
+#pragma unroll 1
+    for (int i0 = t * 16; i0 < NT * 8192; i0 += 512 * 16) {
+        uint4 v[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) v[j] = *reinterpret_cast<const uint4 *>(src + i0 + j * 128 * 16);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            *reinterpret_cast<uint4 *>(dst + i0 + j * 128 * 16) = chunk_bf16_to_f16(v[j], amax);
+    }
+}
+
 __device__ __forceinline__ uint32_t lane_addr(uint32_t tbase, int quad, uint32_t col)
 {
     return tbase + (static_cast<uint32_t>(quad * 32) << 16) + col;
@@ -238,9 +254,12 @@ __device__ __forceinline__ void producer(const GdnArgs &a, const CUtensorMap *tm
     const uint32_t bar_id = 1 + p;
     uint8_t *in = sm + kPOffIn + p * kPIn;
     uint8_t *out = sm + kPOffOut + p * kOutBytes;
+    // A and then T = (I + A)^{-1} share one array: every block of A is dead
+    // before the same block of T is written, and A's zero upper triangle is
+    // exactly the zero upper blocks the merges read.
     float *As = reinterpret_cast<float *>(sm + kPOffAT + p * kPAT);
-    float *Ts = As + kC * kLdA;
-    float *Xs = Ts + kC * kLdA;
+    float *Ts = As;
+    float *Xs = As + kC * kLdA;
     float *gout = reinterpret_cast<float *>(out + kOutG);
     const uint32_t tcol = tbase + p * 64;            // [K;Q] K^T
     const uint32_t r_full =
@@ -269,11 +288,6 @@ __device__ __forceinline__ void producer(const GdnArgs &a, const CUtensorMap *tm
             }
         }
     };
-    // upper blocks of T that no phase writes but the merges read: zero once
-    for (int idx = t; idx < 2 * 16 * 16; idx += 128) {
-        const int b = idx >> 8, r = (idx >> 4) & 15, cc = idx & 15;
-        Ts[(32 * b + r) * kLdA + 32 * b + 16 + cc] = 0.f;
-    }
     if (p < nchunks && t == 0) issue_in(p);
     load_gates(p);
 
@@ -332,10 +346,10 @@ __device__ __forceinline__ void producer(const GdnArgs &a, const CUtensorMap *tm
             }
             mma_commit(&s->mma[p]);
         }
+        // while it runs: fp16 copies of the K and Q tiles, shipped to the consumer
+        convert_copy_tiles<4>(in, out + kOutKQ, t, &amax);
         wait_bar(&s->mma[p], k & 1, false, abort_flag, a.status);
         tc_fence_after();
-        // the q/k buffer is free: fetch the pipeline's next chunk
-        if (t == 0 && c + 2 < nchunks && !*abort_flag) issue_in(c + 2);
 
         // A (fp32, rows 0-63) and P (fp16, rows 64-127).  The decay factor
         // e^{g_i - g_j} splits as e^{g_i - g_r} e^{g_r - g_j} around the middle
@@ -399,8 +413,11 @@ __device__ __forceinline__ void producer(const GdnArgs &a, const CUtensorMap *tm
                 }
             }
         }
+        fence_async_smem();  // our reads of the q/k buffer precede its next TMA write
         tc_fence_before();
         named_sync(bar_id, 128);
+        // the q/k buffer is free (MMA done, copies made): fetch the next chunk
+        if (t == 0 && c + 2 < nchunks && !*abort_flag) issue_in(c + 2);
 
         // T = (I + A)^{-1}
         // (1) 16x16 diagonal blocks: warp `quad` owns block `quad`, lane l < 16
@@ -418,6 +435,7 @@ __device__ __forceinline__ void producer(const GdnArgs &a, const CUtensorMap *tm
                     if (m >= l) acc = fmaf(As[(16 * b + r) * kLdA + 16 * b + m], tv[m], acc);
                 if (r > l) tv[r] = -acc;
             }
+            __syncwarp();  // every lane has read its A block before T overwrites it
             if (l < 16) {
 #pragma unroll
                 for (int r = 0; r < 16; ++r) Ts[(16 * b + r) * kLdA + 16 * b + l] = tv[r];
@@ -548,12 +566,9 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
     auto issue_qkv = [&](int c) {
         uint8_t *slot = sm + (c & 1) * kSlotBytes;
         const int z = (int)(start + (long)c * kC);
-        mbar_arrive_expect_tx(&s->tma[c & 1], 6 * 8192);
-        for (int b = 0; b < 2; ++b) {
-            tma_load_3d(slot + kSlotQ + b * 8192, tm_q, &s->tma[c & 1], b * 64, h, z);
-            tma_load_3d(slot + kSlotK + b * 8192, tm_k, &s->tma[c & 1], b * 64, h, z);
+        mbar_arrive_expect_tx(&s->tma[c & 1], 2 * 8192);
+        for (int b = 0; b < 2; ++b)
             tma_load_3d(slot + kSlotV + b * 8192, tm_v, &s->tma[c & 1], v0 + b * 64, h, z);
-        }
     };
 
     if (tid < 128) {
@@ -581,7 +596,7 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
             uint8_t *slot = sm + (c & 1) * kSlotBytes;
             const uint32_t id_w = idesc_f16_f32(128, 64, 1, 0);
             const uint32_t sa = smem_u32(slot);
-            const uint64_t dk = sdesc_sw128(sa + kSlotK, 8192, 1024);
+            const uint64_t dk = sdesc_sw128(sa + kOutKQ, 16384, 1024);
             const uint64_t dtpp = sdesc_sw128(sa + kOutTpp, 16, 1024);
             const uint64_t dv = sdesc_sw128(sa + kSlotV, 8192, 1024);
             const uint64_t dtp = sdesc_sw128(sa + kOutTp, 16, 1024);
@@ -652,12 +667,12 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
                 const uint32_t sa = smem_u32(slot);
                 const uint64_t ds = sdesc_sw128(smem_u32(Sb), 16, 1024);
                 const uint64_t dw = sdesc_sw128(smem_u32(Wt), 8192, 1024);
-                const uint64_t dq = sdesc_sw128(sa + kSlotQ, 16, 1024);
+                const uint64_t dq = sdesc_sw128(sa + kOutKQ + 8192, 16, 1024);
                 const uint32_t csq = tbase + kColSQ + sl * 64;
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
                     const uint32_t oa = ((ks >> 2) * 16384 + (ks & 3) * 32) >> 4;
-                    const uint32_t oq = ((ks >> 2) * 8192 + (ks & 3) * 32) >> 4;
+                    const uint32_t oq = oa;
                     mma_f16kind(tbase + kColSW, ds + oa, dw + ks * (2048 >> 4), id_w, ks > 0);
                     mma_f16kind(csq, ds + oa, dq + oq, id_q, ks > 0);
                 }
@@ -699,7 +714,7 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
                 const uint64_t dvn = sdesc_sw128(smem_u32(VnT), 16, 1024);
                 const uint64_t dp = sdesc_sw128(sa + kOutP, 16, 1024);
                 const uint64_t dvs = sdesc_sw128(sa + kSlotV, 16, 1024);
-                const uint64_t dk = sdesc_sw128(sa + kSlotK, 8192, 1024);
+                const uint64_t dk = sdesc_sw128(sa + kOutKQ, 16384, 1024);
                 const uint32_t co = tbase + kColO + sl * 64;
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks) {
@@ -741,7 +756,7 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
             uint8_t *slot = sm + sl * kSlotBytes;
             const int nc = (int)min((long)kC, len - (long)c * kC);
             wait_bar(&s->tma[sl], (c >> 1) & 1, false, abort_flag, a.status);
-            convert_tiles<6>(slot + kSlotQ, nc, t, &amax);  // Q, K, V are contiguous
+            convert_tiles<2>(slot + kSlotV, nc, t, &amax);  // V, both d_v halves
             fence_async_smem();
             mbar_arrive(&s->conv[sl]);
         };
