@@ -233,25 +233,11 @@ __device__ __noinline__ bool wait_cluster(uint64_t *bar, uint32_t parity, volati
     }
 }
 
-// Single-thread wait.
-__device__ __forceinline__ bool wait_one(uint64_t *bar, uint32_t parity, bool cluster_scope,
+__device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, bool cluster_scope,
                                          volatile int *abort_flag, unsigned int *status)
 {
     return cluster_scope ? wait_cluster(bar, parity, abort_flag, status)
                          : wait_cta(bar, parity, abort_flag, status);
-}
-
-// Warp-uniform wait: lane 0 polls the barrier, the warp then proceeds
-// together.  Keeps polling traffic off the shared memory the tensor core is
-// reading operands from.
-__device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, bool cluster_scope,
-                                         volatile int *abort_flag, unsigned int *status)
-{
-    int ok = 0;
-    if ((threadIdx.x & 31) == 0) ok = wait_one(bar, parity, cluster_scope, abort_flag, status);
-    ok = __shfl_sync(0xffffffffu, ok, 0);
-    __syncwarp();
-    return ok != 0;
 }
 
 // ======================================================================
@@ -550,7 +536,7 @@ __device__ __forceinline__ void producer(const GdnArgs &a, const CUtensorMap *tm
 
         // ship P, T', T'' and the decay vectors once the consumer's slot is free
         if (t == 0) {
-            if (wait_one(&s->slot_empty[p], (k + 1) & 1, true, abort_flag, a.status)) {
+            if (wait_bar(&s->slot_empty[p], (k + 1) & 1, true, abort_flag, a.status)) {
                 mbar_arrive_expect_tx_remote(r_full, kOutBytes);
                 bulk_copy_to_peer(r_slot, out, kOutBytes, r_full);
             }
