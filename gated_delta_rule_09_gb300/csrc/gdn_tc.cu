@@ -724,17 +724,20 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
                 mma_commit(&s->mma2);
                 mma_commit(&s->out_full[sl]);
             }
-            if (c + 1 < nchunks) {  // next chunk's W^T, U^T (their columns are free now)
-                wait_bar(&s->full[sl ^ 1], ((c + 1) >> 1) & 1, true, abort_flag, a.status);
-                wait_bar(&s->conv[sl ^ 1], ((c + 1) >> 1) & 1, false, abort_flag, a.status);
-                if (t == 0) issue_wu(c + 1);
-            }
             wait_bar(&s->mma2, c & 1, false, abort_flag, a.status);
             tc_fence_after();
             // slot consumed: hand it back to the producer, refill our tiles
             if (t == 0) {
                 mbar_arrive_remote(r_slot_empty + sl * sizeof(uint64_t));
                 if (c + 2 < nchunks && !*abort_flag) issue_qkv(c + 2);
+            }
+            if (c + 1 < nchunks) {  // next chunk's W^T, U^T (their columns are free now)
+                wait_bar(&s->full[sl ^ 1], ((c + 1) >> 1) & 1, true, abort_flag, a.status);
+                wait_bar(&s->conv[sl ^ 1], ((c + 1) >> 1) & 1, false, abort_flag, a.status);
+                if (t == 0) {
+                    tc_fence_after();
+                    issue_wu(c + 1);
+                }
             }
         }
         if (a.S_final && !*abort_flag) {
