@@ -54,7 +54,7 @@ using namespace sm100;
 constexpr int kC = 64;       // chunk length
 constexpr int kDK = 128;     // d_k
 constexpr int kDVT = 128;    // d_v columns per unit
-constexpr int kThreads = 256;
+constexpr int kThreads = 288;  // 8 working warps + a mailbox warp on the consumer
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
 constexpr float kF16Max = 65504.f;
 constexpr int kLdA = 65;     // padded fp32 row stride of A / T
@@ -250,6 +250,7 @@ __device__ __forceinline__ void producer(const GdnArgs &a, const CUtensorMap *tm
     PSmall *s = reinterpret_cast<PSmall *>(sm + kPOffSmall);
     volatile int *abort_flag = &s->abort_flag;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (warp >= 8) return;  // the mailbox warp only works on the consumer
     const int p = warp >> 2, quad = warp & 3, t = tid & 127;
     const uint32_t bar_id = 1 + p;
     uint8_t *in = sm + kPOffIn + p * kPIn;
@@ -622,7 +623,6 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
             wait_bar(&s->full[sl], kk & 1, true, abort_flag, a.status);
             wait_bar(&s->conv[sl], kk & 1, false, abort_flag, a.status);
             wait_bar(&s->out_done[sl], (kk + 1) & 1, false, abort_flag, a.status);
-            if (t == 0) mbar_arrive_remote(r_src_free + sl * sizeof(uint64_t));
             if (t < kC) {
                 s->egc[sl][t] = gs[kC + t];
                 mbar_arrive(&s->egc_full[sl]);
@@ -748,6 +748,15 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
                 tmem_ld_wait();
 #pragma unroll
                 for (int j = 0; j < 32; ++j) dst[cb * 32 + j] = x[j];
+            }
+        }
+    } else if (tid >= 256) {
+        // ---------------- mailbox (warp 8): tell the producer its outgoing
+        // buffer is free the moment each bulk copy has landed
+        if (tid == 256) {
+            for (int c = 0; c < nchunks; ++c) {
+                if (wait_bar(&s->full[c & 1], (c >> 1) & 1, true, abort_flag, a.status))
+                    mbar_arrive_remote(r_src_free + (c & 1) * sizeof(uint64_t));
             }
         }
     } else {
