@@ -57,7 +57,9 @@ constexpr int kDVT = 128;    // d_v columns per unit
 constexpr int kThreads = 288;  // 8 working warps + a mailbox warp on the consumer
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
 constexpr float kF16Max = 65504.f;
-constexpr int kLdA = 65;     // padded fp32 row stride of A / T
+constexpr int kLdA = 68;     // fp32 row stride of A / T: 16-byte rows, 4-bank offset per row
+constexpr int kLdX2 = 20;    // row stride of the 16x16 merge scratch
+constexpr int kLdX3 = 36;    // row stride of the 32x32 merge scratch
 
 // ---- a ring slot: what the producer ships, then the consumer's own tiles
 constexpr int kOutP = 0;           // P rows i (K-major), fp16
@@ -71,7 +73,7 @@ constexpr int kSlotBytes = kSlotV + 16384;
 
 // ---- producer shared memory (per pipeline p = 0, 1)
 constexpr int kPIn = 32768;                        // [K | Q] per d_k half, bf16 (TMA)
-constexpr int kPAT = 21504;                        // fp32 A then T in place [64][65] | X[32][33]
+constexpr int kPAT = 22528;                        // fp32 A then T in place [64][68] | X[32][36]
 constexpr int kPOffIn = 0;
 constexpr int kPOffOut = kPOffIn + 2 * kPIn;
 constexpr int kPOffAT = kPOffOut + 2 * kOutBytes;
@@ -81,12 +83,12 @@ constexpr int kCOffW = 2 * kSlotBytes;             // W^T rows d (MN-major B ope
 constexpr int kCOffSb = kCOffW + 16384;            // S as fp16, 2 d_k halves x 128 rows
 constexpr int kCOffVnT = kCOffSb + 32768;          // V_new^T rows v (K-major), fp16
 constexpr int kCOffSmall = kCOffVnT + 16384;
-constexpr int kSmallBytes = 2048;
+constexpr int kSmallBytes = 3072;
 constexpr int kSmemBytes =
     (kCOffSmall > kPOffSmall ? kCOffSmall : kPOffSmall) + kSmallBytes + 1024;
 
 struct PSmall {
-    float scan[2][kC], beta[2][kC], colf[2][kC];
+    float scan[2][kC], beta[2][kC], colf[2][kC], colb[2][kC];
     uint64_t tma_in[2], mma[2], src_free[2], slot_empty[2];
     uint32_t tmem;
     int abort_flag;
@@ -319,6 +321,7 @@ __device__ __forceinline__ void producer(const GdnArgs &a, const CUtensorMap *tm
             gout[kC + t] = __expf(gout[t]);
             gout[2 * kC + t] = __expf(gC - gout[t]);
             s->colf[p][t] = __expf(gout[31] - gout[t]);
+            s->colb[p][t] = s->beta[p][t] * gout[kC + t];  // beta e^g
         }
 
         // q/k tiles (bf16: K K^T and Q K^T are exact products); rows past the
@@ -371,7 +374,9 @@ __device__ __forceinline__ void producer(const GdnArgs &a, const CUtensorMap *tm
                 if (half == 1 && quad % 2 == 0) {  // rows 0-31 of A / P: all j >= 32 are zero
                     if (is_k) {
 #pragma unroll
-                        for (int jj = 0; jj < 32; ++jj) As[i * kLdA + 32 + jj] = 0.f;
+                        for (int q = 0; q < 8; ++q)
+                            *reinterpret_cast<float4 *>(As + i * kLdA + 32 + 4 * q) =
+                                make_float4(0.f, 0.f, 0.f, 0.f);
                     } else {
 #pragma unroll
                         for (int jj = 0; jj < 32; ++jj) x[jj] = 0.f;
@@ -406,7 +411,9 @@ __device__ __forceinline__ void producer(const GdnArgs &a, const CUtensorMap *tm
                 }
                 if (is_k) {
 #pragma unroll
-                    for (int jj = 0; jj < 32; ++jj) As[i * kLdA + half * 32 + jj] = x[jj];
+                    for (int q = 0; q < 8; ++q)
+                        *reinterpret_cast<float4 *>(As + i * kLdA + half * 32 + 4 * q) =
+                            make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
                 } else {
 #pragma unroll
                     for (int q = 0; q < 4; ++q)
@@ -450,69 +457,63 @@ __device__ __forceinline__ void producer(const GdnArgs &a, const CUtensorMap *tm
         {
             const int pp = t >> 6, r = (t & 63) >> 2, c4 = (t & 3) * 4;
             const int R = 16 * (2 * pp + 1), Cc = 32 * pp;
-            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
             for (int m = 0; m < 16; ++m) {
                 const float av = As[(R + r) * kLdA + Cc + m];
-                const float *tr = Ts + (Cc + m) * kLdA + Cc + c4;
-#pragma unroll
-                for (int e = 0; e < 4; ++e) acc[e] = fmaf(av, tr[e], acc[e]);
+                const float4 tv = *reinterpret_cast<const float4 *>(Ts + (Cc + m) * kLdA + Cc + c4);
+                acc.x = fmaf(av, tv.x, acc.x);
+                acc.y = fmaf(av, tv.y, acc.y);
+                acc.z = fmaf(av, tv.z, acc.z);
+                acc.w = fmaf(av, tv.w, acc.w);
             }
-#pragma unroll
-            for (int e = 0; e < 4; ++e) Xs[pp * 16 * 17 + r * 17 + c4 + e] = acc[e];
+            *reinterpret_cast<float4 *>(Xs + pp * 16 * kLdX2 + r * kLdX2 + c4) = acc;
             named_sync(bar_id, 128);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) acc[e] = 0.f;
+            acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
             for (int m = 0; m < 16; ++m) {
                 const float tv = Ts[(R + r) * kLdA + R + m];
-                const float *xr = Xs + pp * 16 * 17 + m * 17 + c4;
-#pragma unroll
-                for (int e = 0; e < 4; ++e) acc[e] = fmaf(tv, xr[e], acc[e]);
+                const float4 xv = *reinterpret_cast<const float4 *>(Xs + pp * 16 * kLdX2 + m * kLdX2 + c4);
+                acc.x = fmaf(tv, xv.x, acc.x);
+                acc.y = fmaf(tv, xv.y, acc.y);
+                acc.z = fmaf(tv, xv.z, acc.z);
+                acc.w = fmaf(tv, xv.w, acc.w);
             }
-#pragma unroll
-            for (int e = 0; e < 4; ++e) Ts[(R + r) * kLdA + Cc + c4 + e] = -acc[e];
+            *reinterpret_cast<float4 *>(Ts + (R + r) * kLdA + Cc + c4) =
+                make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
         }
         named_sync(bar_id, 128);
         // (3) 32 -> 64: T[32:64, 0:32] = -T2 (A21 T1); each thread a 2x4 block.
         {
             const int r2 = (t >> 3) * 2, c4 = (t & 7) * 4;
-            float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+            float4 a0c = make_float4(0.f, 0.f, 0.f, 0.f), a1c = a0c;
 #pragma unroll 8
             for (int m = 0; m < 32; ++m) {
                 const float a0 = As[(32 + r2) * kLdA + m], a1 = As[(33 + r2) * kLdA + m];
-                const float *tr = Ts + m * kLdA + c4;
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float tv = tr[e];
-                    acc[0][e] = fmaf(a0, tv, acc[0][e]);
-                    acc[1][e] = fmaf(a1, tv, acc[1][e]);
-                }
+                const float4 tv = *reinterpret_cast<const float4 *>(Ts + m * kLdA + c4);
+                a0c.x = fmaf(a0, tv.x, a0c.x); a0c.y = fmaf(a0, tv.y, a0c.y);
+                a0c.z = fmaf(a0, tv.z, a0c.z); a0c.w = fmaf(a0, tv.w, a0c.w);
+                a1c.x = fmaf(a1, tv.x, a1c.x); a1c.y = fmaf(a1, tv.y, a1c.y);
+                a1c.z = fmaf(a1, tv.z, a1c.z); a1c.w = fmaf(a1, tv.w, a1c.w);
             }
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                Xs[r2 * 33 + c4 + e] = acc[0][e];
-                Xs[(r2 + 1) * 33 + c4 + e] = acc[1][e];
-            }
+            *reinterpret_cast<float4 *>(Xs + r2 * kLdX3 + c4) = a0c;
+            *reinterpret_cast<float4 *>(Xs + (r2 + 1) * kLdX3 + c4) = a1c;
             named_sync(bar_id, 128);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) acc[0][e] = acc[1][e] = 0.f;
+            a0c = make_float4(0.f, 0.f, 0.f, 0.f);
+            a1c = a0c;
 #pragma unroll 8
             for (int m = 0; m < 32; ++m) {
                 const float t0 = Ts[(32 + r2) * kLdA + 32 + m], t1 = Ts[(33 + r2) * kLdA + 32 + m];
-                const float *xr = Xs + m * 33 + c4;
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float xv = xr[e];
-                    acc[0][e] = fmaf(t0, xv, acc[0][e]);
-                    acc[1][e] = fmaf(t1, xv, acc[1][e]);
-                }
+                const float4 xv = *reinterpret_cast<const float4 *>(Xs + m * kLdX3 + c4);
+                a0c.x = fmaf(t0, xv.x, a0c.x); a0c.y = fmaf(t0, xv.y, a0c.y);
+                a0c.z = fmaf(t0, xv.z, a0c.z); a0c.w = fmaf(t0, xv.w, a0c.w);
+                a1c.x = fmaf(t1, xv.x, a1c.x); a1c.y = fmaf(t1, xv.y, a1c.y);
+                a1c.z = fmaf(t1, xv.z, a1c.z); a1c.w = fmaf(t1, xv.w, a1c.w);
             }
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                Ts[(32 + r2) * kLdA + c4 + e] = -acc[0][e];
-                Ts[(33 + r2) * kLdA + c4 + e] = -acc[1][e];
-            }
+            *reinterpret_cast<float4 *>(Ts + (32 + r2) * kLdA + c4) =
+                make_float4(-a0c.x, -a0c.y, -a0c.z, -a0c.w);
+            *reinterpret_cast<float4 *>(Ts + (33 + r2) * kLdA + c4) =
+                make_float4(-a1c.x, -a1c.y, -a1c.z, -a1c.w);
         }
         named_sync(bar_id, 128);
         // T'' = T diag(beta e^g) and T' = T diag(beta), both shipped
@@ -520,15 +521,18 @@ __device__ __forceinline__ void producer(const GdnArgs &a, const CUtensorMap *tm
             const bool first = t < kC;
             const int j = first ? t : t - kC;
             uint8_t *dst = first ? out + kOutTpp : out + kOutTp;
+            const float *scale = first ? s->colb[p] : s->beta[p];
             float x[8];
 #pragma unroll 1
             for (int q = 0; q < 8; ++q) {
+                const float4 t0 = *reinterpret_cast<const float4 *>(Ts + j * kLdA + q * 8);
+                const float4 t1 = *reinterpret_cast<const float4 *>(Ts + j * kLdA + q * 8 + 4);
+                const float4 s0 = *reinterpret_cast<const float4 *>(scale + q * 8);
+                const float4 s1 = *reinterpret_cast<const float4 *>(scale + q * 8 + 4);
+                x[0] = t0.x * s0.x; x[1] = t0.y * s0.y; x[2] = t0.z * s0.z; x[3] = t0.w * s0.w;
+                x[4] = t1.x * s1.x; x[5] = t1.y * s1.y; x[6] = t1.z * s1.z; x[7] = t1.w * s1.w;
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const int cc = q * 8 + e;
-                    const float sc = first ? s->beta[p][cc] * gout[kC + cc] : s->beta[p][cc];
-                    x[e] = (cc <= j) ? Ts[j * kLdA + cc] * sc : 0.f;
-                }
+                for (int e = 0; e < 8; ++e) x[e] = (q * 8 + e <= j) ? x[e] : 0.f;
                 st_chunk(dst, j, q, x, &amax);
             }
         }
