@@ -66,9 +66,11 @@ constexpr int kOutP = 0;           // P rows i (K-major), fp16
 constexpr int kOutTp = 8192;       // T' = T diag(beta) rows j (K-major), fp16
 constexpr int kOutTpp = 16384;     // T'' = T diag(beta e^g) rows j (K-major), fp16
 constexpr int kOutG = 24576;       // g[64], e^g[64], e^{g_C-g}[64] fp32
-constexpr int kOutKQ = 25600;      // fp16 [K rows | Q rows] per d_k half (2 x 16 KB)
-constexpr int kOutBytes = 58368;   // shipped per chunk
-constexpr int kSlotV = kOutBytes;          // V, 2 d_v halves (later V_new * e^{g_C-g})
+constexpr int kOutBytes = 25600;   // shipped per chunk (distributed shared memory moves
+                                   // ~20 bytes per cycle, so only what the consumer
+                                   // cannot load itself is shipped)
+constexpr int kSlotKQ = kOutBytes;         // [K rows | Q rows] per d_k half, fp16 after conversion
+constexpr int kSlotV = kSlotKQ + 32768;    // V, 2 d_v halves (later V_new * e^{g_C-g})
 constexpr int kSlotBytes = kSlotV + 16384;
 
 // ---- producer shared memory (per pipeline p = 0, 1)
@@ -173,23 +175,6 @@ __device__ __forceinline__ void convert_tiles(uint8_t *base, int nc, int t, floa
         for (int j = 0; j < 4; ++j)
             *reinterpret_cast<uint4 *>(ptr[j]) =
                 keep[j] ? chunk_bf16_to_f16(v[j], amax) : make_uint4(0, 0, 0, 0);
-    }
-}
-
-// bf16 -> fp16 copy of NT 64-row x 128-byte tiles from `src` to `dst` (same
-// swizzled positions), four 16-byte chunks per thread at a time.
-template <int NT>
-__device__ __forceinline__ void convert_copy_tiles(const uint8_t *src, uint8_t *dst, int t,
-                                                   float *amax)
-{
-#pragma unroll 1
-    for (int i0 = t * 16; i0 < NT * 8192; i0 += 512 * 16) {
-        uint4 v[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) v[j] = *reinterpret_cast<const uint4 *>(src + i0 + j * 128 * 16);
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-            *reinterpret_cast<uint4 *>(dst + i0 + j * 128 * 16) = chunk_bf16_to_f16(v[j], amax);
     }
 }
 
@@ -350,8 +335,6 @@ __device__ __forceinline__ void producer(const GdnArgs &a, const CUtensorMap *tm
             }
             mma_commit(&s->mma[p]);
         }
-        // while it runs: fp16 copies of the K and Q tiles, shipped to the consumer
-        convert_copy_tiles<4>(in, out + kOutKQ, t, &amax);
         wait_bar(&s->mma[p], k & 1, false, abort_flag, a.status);
         tc_fence_after();
 
@@ -421,10 +404,9 @@ __device__ __forceinline__ void producer(const GdnArgs &a, const CUtensorMap *tm
                 }
             }
         }
-        fence_async_smem();  // our reads of the q/k buffer precede its next TMA write
         tc_fence_before();
         named_sync(bar_id, 128);
-        // the q/k buffer is free (MMA done, copies made): fetch the next chunk
+        // the q/k buffer is free (its MMA is done): fetch the next chunk
         if (t == 0 && c + 2 < nchunks && !*abort_flag) issue_in(c + 2);
 
         // T = (I + A)^{-1}
@@ -571,9 +553,12 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
     auto issue_qkv = [&](int c) {
         uint8_t *slot = sm + (c & 1) * kSlotBytes;
         const int z = (int)(start + (long)c * kC);
-        mbar_arrive_expect_tx(&s->tma[c & 1], 2 * 8192);
-        for (int b = 0; b < 2; ++b)
+        mbar_arrive_expect_tx(&s->tma[c & 1], 6 * 8192);
+        for (int b = 0; b < 2; ++b) {
+            tma_load_3d(slot + kSlotKQ + b * 16384, tm_k, &s->tma[c & 1], b * 64, h, z);
+            tma_load_3d(slot + kSlotKQ + b * 16384 + 8192, tm_q, &s->tma[c & 1], b * 64, h, z);
             tma_load_3d(slot + kSlotV + b * 8192, tm_v, &s->tma[c & 1], v0 + b * 64, h, z);
+        }
     };
 
     if (tid < 128) {
@@ -601,7 +586,7 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
             uint8_t *slot = sm + (c & 1) * kSlotBytes;
             const uint32_t id_w = idesc_f16_f32(128, 64, 1, 0);
             const uint32_t sa = smem_u32(slot);
-            const uint64_t dk = sdesc_sw128(sa + kOutKQ, 16384, 1024);
+            const uint64_t dk = sdesc_sw128(sa + kSlotKQ, 16384, 1024);
             const uint64_t dtpp = sdesc_sw128(sa + kOutTpp, 16, 1024);
             const uint64_t dv = sdesc_sw128(sa + kSlotV, 8192, 1024);
             const uint64_t dtp = sdesc_sw128(sa + kOutTp, 16, 1024);
@@ -671,7 +656,7 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
                 const uint32_t sa = smem_u32(slot);
                 const uint64_t ds = sdesc_sw128(smem_u32(Sb), 16, 1024);
                 const uint64_t dw = sdesc_sw128(smem_u32(Wt), 8192, 1024);
-                const uint64_t dq = sdesc_sw128(sa + kOutKQ + 8192, 16, 1024);
+                const uint64_t dq = sdesc_sw128(sa + kSlotKQ + 8192, 16, 1024);
                 const uint32_t csq = tbase + kColSQ + sl * 64;
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
@@ -718,7 +703,7 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
                 const uint64_t dvn = sdesc_sw128(smem_u32(VnT), 16, 1024);
                 const uint64_t dp = sdesc_sw128(sa + kOutP, 16, 1024);
                 const uint64_t dvs = sdesc_sw128(sa + kSlotV, 16, 1024);
-                const uint64_t dk = sdesc_sw128(sa + kOutKQ, 16384, 1024);
+                const uint64_t dk = sdesc_sw128(sa + kSlotKQ, 16384, 1024);
                 const uint32_t co = tbase + kColO + sl * 64;
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks) {
@@ -772,7 +757,7 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
             uint8_t *slot = sm + sl * kSlotBytes;
             const int nc = (int)min((long)kC, len - (long)c * kC);
             wait_bar(&s->tma[sl], (c >> 1) & 1, false, abort_flag, a.status);
-            convert_tiles<2>(slot + kSlotV, nc, t, &amax);  // V, both d_v halves
+            convert_tiles<6>(slot + kSlotKQ, nc, t, &amax);  // K, Q (both halves), V
             fence_async_smem();
             mbar_arrive(&s->conv[sl]);
         };
