@@ -537,6 +537,7 @@ __device__ __forceinline__ void producer(const GdnArgs &a, const CUtensorMap *tm
 // ======================================================================
 __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm_q,
                                          const CUtensorMap *tm_k, const CUtensorMap *tm_v,
+                                         const CUtensorMap *tm_o,
                                          uint8_t *sm, uint32_t tbase, long start, long len,
                                          int nchunks, int h, int n, int v0)
 {
@@ -716,10 +717,9 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
             wait_bar(&s->mma2, c & 1, false, abort_flag, a.status);
             tc_fence_after();
             // slot consumed: hand it back to the producer, refill our tiles
-            if (t == 0) {
-                mbar_arrive_remote(r_slot_empty + sl * sizeof(uint64_t));
-                if (c + 2 < nchunks && !*abort_flag) issue_qkv(c + 2);
-            }
+            // our q/k/v tiles are consumed: refill them (the shipped part of
+            // the slot is handed back by warps 4-7 once the outputs are out)
+            if (t == 0 && c + 2 < nchunks && !*abort_flag) issue_qkv(c + 2);
             if (c + 1 < nchunks) {  // next chunk's W^T, U^T (their columns are free now)
                 wait_bar(&s->full[sl ^ 1], ((c + 1) >> 1) & 1, true, abort_flag, a.status);
                 wait_bar(&s->conv[sl ^ 1], ((c + 1) >> 1) & 1, false, abort_flag, a.status);
@@ -761,30 +761,59 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
             fence_async_smem();
             mbar_arrive(&s->conv[sl]);
         };
+        // o_i = e^{g_i} (S Q^T)_i + O_intra,i.  A full chunk is staged as a
+        // [64 tokens][128 d_v] bf16 tile in the slot's P|T' region (free once
+        // the chunk's second MMA batch is done) and written with two TMA
+        // stores; a partial chunk (the end of a sequence) uses plain stores so
+        // nothing lands in the next sequence.  The slot goes back to the
+        // producer after that.
         auto output = [&](int c) {
             const int sl = c & 1;
+            uint8_t *slot = sm + sl * kSlotBytes;
             const int nc = (int)min((long)kC, len - (long)c * kC);
             const long tok0 = start + (long)c * kC;
             wait_bar(&s->egc_full[sl], (c >> 1) & 1, false, abort_flag, a.status);
             wait_bar(&s->out_full[sl], (c >> 1) & 1, false, abort_flag, a.status);
             tc_fence_after();
             const size_t col = (size_t)v0 + t;
+            uint8_t *stage = slot + kOutP + (t >> 6) * 8192;  // d_v half of this thread
+            const int vc = (t & 63) >> 3, ve = t & 7;
             float x[32], y[32];
-            #pragma unroll 1
+#pragma unroll 1
             for (int half = 0; half < 2; ++half) {
                 tmem_ld32(lane_addr(tbase, quad, kColSQ + sl * 64 + half * 32), x);
                 tmem_ld32(lane_addr(tbase, quad, kColO + sl * 64 + half * 32), y);
                 tmem_ld_wait();
+                if (nc == kC) {
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const int i = half * 32 + j;
-                    if (i < nc)
-                        o[((size_t)(tok0 + i) * H + h) * dv + col] =
+                    for (int j = 0; j < 32; ++j) {
+                        const int i = half * 32 + j;
+                        reinterpret_cast<__nv_bfloat16 *>(stage + sw128(i, vc))[ve] =
                             __float2bfloat16_rn(fmaf(s->egc[sl][i], x[j], y[j]));
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const int i = half * 32 + j;
+                        if (i < nc)
+                            o[((size_t)(tok0 + i) * H + h) * dv + col] =
+                                __float2bfloat16_rn(fmaf(s->egc[sl][i], x[j], y[j]));
+                    }
                 }
             }
             tc_fence_before();
             mbar_arrive(&s->out_done[sl]);
+            if (nc == kC) {
+                fence_async_smem();
+                named_sync(2, 128);
+                if (t == 0) {
+                    tma_store_3d(tm_o, slot + kOutP, v0, h, (int)tok0);
+                    tma_store_3d(tm_o, slot + kOutP + 8192, v0 + 64, h, (int)tok0);
+                    bulk_commit();
+                    bulk_wait_read();
+                }
+            }
+            if (t == 0) mbar_arrive_remote(r_slot_empty + sl * sizeof(uint64_t));
         };
         auto w_epilogue = [&](int c) {
             wait_bar(&s->w_mma, c & 1, false, abort_flag, a.status);
@@ -811,13 +840,15 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
             output(c - 1);
         }
         if (nchunks > 0) output(nchunks - 1);
+        if (t == 0) bulk_wait_all();
     }
     if (amax > kF16Max) atomicOr(a.status, 0x4u);
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 gdn_tc_kernel(const GdnArgs a, const __grid_constant__ CUtensorMap tm_q,
-              const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v)
+              const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+              const __grid_constant__ CUtensorMap tm_o)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>(
@@ -880,6 +911,7 @@ gdn_tc_kernel(const GdnArgs a, const __grid_constant__ CUtensorMap tm_q,
             prefetch_tensormap(&tm_q);
             prefetch_tensormap(&tm_k);
             prefetch_tensormap(&tm_v);
+            prefetch_tensormap(&tm_o);
         }
     }
     if (warp == 0) {
@@ -892,7 +924,7 @@ gdn_tc_kernel(const GdnArgs a, const __grid_constant__ CUtensorMap tm_q,
     const uint32_t tbase = *tmem_slot;
 
     if (rank == 0) producer(a, &tm_q, &tm_k, sm, tbase, start, len, nchunks, h);
-    else consumer(a, &tm_q, &tm_k, &tm_v, sm, tbase, start, len, nchunks, h, n, v0);
+    else consumer(a, &tm_q, &tm_k, &tm_v, &tm_o, sm, tbase, start, len, nchunks, h, n, v0);
 
     tc_fence_before();
     __syncthreads();
@@ -945,15 +977,15 @@ bool gdn_tc_supported(const GdnArgs &a)
 cudaError_t gdn_launch_tc(const GdnArgs &a, cudaStream_t s, int *launches)
 {
     const long tokens = a.cu_seqlens ? (long)a.T : (long)a.N * a.T;
-    CUtensorMap mq, mk, mv;
+    CUtensorMap mq, mk, mv, mo;
     if (!make_map(&mq, a.q, tokens, a.H, a.dk) || !make_map(&mk, a.k, tokens, a.H, a.dk) ||
-        !make_map(&mv, a.v, tokens, a.H, a.dv))
+        !make_map(&mv, a.v, tokens, a.H, a.dv) || !make_map(&mo, a.o, tokens, a.H, a.dv))
         return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(gdn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          kSmemBytes);
     if (e != cudaSuccess) return e;
     dim3 grid(2 * (a.dv / kDVT), a.H, a.N);
-    gdn_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(a, mq, mk, mv);
+    gdn_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(a, mq, mk, mv, mo);
     *launches = 1;
     return cudaGetLastError();
 }
