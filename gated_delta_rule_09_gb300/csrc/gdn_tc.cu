@@ -54,7 +54,7 @@ using namespace sm100;
 constexpr int kC = 64;       // chunk length
 constexpr int kDK = 128;     // d_k
 constexpr int kDVT = 128;    // d_v columns per unit
-constexpr int kThreads = 288;  // 8 working warps + a mailbox warp on the consumer
+constexpr int kThreads = 384;  // producer: 2 x 4 warps (warps 8-11 idle); consumer: 3 x 4 warps
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
 constexpr float kF16Max = 65504.f;
 constexpr int kLdA = 68;     // fp32 row stride of A / T: 16-byte rows, 4-bank offset per row
@@ -77,8 +77,8 @@ constexpr int kSlotBytes = kSlotV + 16384;
 constexpr int kPIn = 32768;                        // [K | Q] per d_k half, bf16 (TMA)
 constexpr int kPAT = 22528;                        // fp32 A then T in place [64][68] | X[32][36]
 constexpr int kPOffIn = 0;
-constexpr int kPOffOut = kPOffIn + 2 * kPIn;
-constexpr int kPOffAT = kPOffOut + 2 * kOutBytes;
+constexpr int kPOffOut = kPOffIn + 2 * kPIn;        // 2 pipelines x 2 outgoing buffers
+constexpr int kPOffAT = kPOffOut + 4 * kOutBytes;
 constexpr int kPOffSmall = kPOffAT + 2 * kPAT;
 // ---- consumer shared memory
 constexpr int kCOffW = 2 * kSlotBytes;             // W^T rows d (MN-major B operand), fp16
@@ -91,7 +91,7 @@ constexpr int kSmemBytes =
 
 struct PSmall {
     float scan[2][kC], beta[2][kC], colf[2][kC], colb[2][kC];
-    uint64_t tma_in[2], mma[2], src_free[2], slot_empty[2];
+    uint64_t tma_in[2], mma[2], slot_empty[2];
     uint32_t tmem;
     int abort_flag;
 };
@@ -237,18 +237,18 @@ __device__ __forceinline__ void producer(const GdnArgs &a, const CUtensorMap *tm
     PSmall *s = reinterpret_cast<PSmall *>(sm + kPOffSmall);
     volatile int *abort_flag = &s->abort_flag;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    if (warp >= 8) return;  // the mailbox warp only works on the consumer
+    if (warp >= 8) return;  // two 4-warp pipelines
     const int p = warp >> 2, quad = warp & 3, t = tid & 127;
     const uint32_t bar_id = 1 + p;
     uint8_t *in = sm + kPOffIn + p * kPIn;
-    uint8_t *out = sm + kPOffOut + p * kOutBytes;
+    uint8_t *out_base = sm + kPOffOut + p * 2 * kOutBytes;
     // A and then T = (I + A)^{-1} share one array: every block of A is dead
     // before the same block of T is written, and A's zero upper triangle is
     // exactly the zero upper blocks the merges read.
     float *As = reinterpret_cast<float *>(sm + kPOffAT + p * kPAT);
     float *Ts = As;
     float *Xs = As + kC * kLdA;
-    float *gout = reinterpret_cast<float *>(out + kOutG);
+
     const uint32_t tcol = tbase + p * 64;            // [K;Q] K^T
     const uint32_t r_full =
         mapa_shared(sm + kCOffSmall + offsetof(CSmall, full) + p * sizeof(uint64_t), 1);
@@ -282,8 +282,11 @@ __device__ __forceinline__ void producer(const GdnArgs &a, const CUtensorMap *tm
     int k = 0;
     for (int c = p; c < nchunks; c += 2, ++k) {
         const int nc = (int)min((long)kC, len - (long)c * kC);
-        // the consumer has received this buffer's previous contents
-        wait_bar(&s->src_free[p], (k + 1) & 1, true, abort_flag, a.status);
+        // Two outgoing buffers per pipeline: by the time a buffer is rewritten
+        // (this pipeline's chunk c - 4), the consumer has finished chunk c - 4,
+        // so the bulk copy out of it is long complete.
+        uint8_t *out = out_base + (k & 1) * kOutBytes;
+        float *gout = reinterpret_cast<float *>(out + kOutG);
 
         // decay: g = inclusive cumulative sum of log alpha (padding adds 0)
         const float la = la_next, bt = b_next;
@@ -547,7 +550,6 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
     const int quad = warp & 3;
     const int H = a.H, dv = a.dv;
     uint8_t *Sb = sm + kCOffSb, *VnT = sm + kCOffVnT, *Wt = sm + kCOffW;
-    const uint32_t r_src_free = mapa_shared(sm + kPOffSmall + offsetof(PSmall, src_free), 0);
     const uint32_t r_slot_empty = mapa_shared(sm + kPOffSmall + offsetof(PSmall, slot_empty), 0);
     float amax = 0.f;
 
@@ -739,18 +741,11 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
                 for (int j = 0; j < 32; ++j) dst[cb * 32 + j] = x[j];
             }
         }
-    } else if (tid >= 256) {
-        // ---------------- mailbox (warp 8): tell the producer its outgoing
-        // buffer is free the moment each bulk copy has landed
-        if (tid == 256) {
-            for (int c = 0; c < nchunks; ++c) {
-                if (wait_bar(&s->full[c & 1], (c >> 1) & 1, true, abort_flag, a.status))
-                    mbar_arrive_remote(r_src_free + (c & 1) * sizeof(uint64_t));
-            }
-        }
     } else {
-        // ---------------- tile conversion and outputs (warps 4-7)
-        const int t = tid - 128;
+        // ---------------- warps 4-7: tile conversion and W^T rows;
+        //                  warps 8-11: outputs
+        const bool conv_group = tid < 256;
+        const int t = tid & 127;
         __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(a.o);
         auto convert = [&](int c) {
             const int sl = c & 1;
@@ -805,7 +800,7 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
             mbar_arrive(&s->out_done[sl]);
             if (nc == kC) {
                 fence_async_smem();
-                named_sync(2, 128);
+                named_sync(3, 128);
                 if (t == 0) {
                     tma_store_3d(tm_o, slot + kOutP, v0, h, (int)tok0);
                     tma_store_3d(tm_o, slot + kOutP + 8192, v0 + 64, h, (int)tok0);
@@ -830,17 +825,15 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
             tc_fence_before();
             mbar_arrive(&s->w_ready);
         };
-        if (nchunks > 0) {
-            convert(0);
-            w_epilogue(0);
+        if (conv_group) {
+            for (int c = 0; c < nchunks; ++c) {
+                convert(c);
+                w_epilogue(c);
+            }
+        } else {
+            for (int c = 0; c < nchunks; ++c) output(c);
+            if (t == 0) bulk_wait_all();
         }
-        for (int c = 1; c < nchunks; ++c) {
-            convert(c);
-            w_epilogue(c);
-            output(c - 1);
-        }
-        if (nchunks > 0) output(nchunks - 1);
-        if (t == 0) bulk_wait_all();
     }
     if (amax > kF16Max) atomicOr(a.status, 0x4u);
 }
@@ -882,7 +875,6 @@ gdn_tc_kernel(const GdnArgs a, const __grid_constant__ CUtensorMap tm_q,
             for (int i = 0; i < 2; ++i) {
                 mbar_init(&s->tma_in[i], 1);
                 mbar_init(&s->mma[i], 1);
-                mbar_init(&s->src_free[i], 1);
                 mbar_init(&s->slot_empty[i], 1);
             }
             s->abort_flag = 0;
