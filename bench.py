@@ -192,18 +192,24 @@ def barrier(world):
         dist.barrier()
 
 
-def cpu_baseline(w, x, sample_tokens):
-    """Oracle on one sequence x all heads x the first ``sample_tokens`` tokens."""
+def cpu_baseline(w, x, sample_tokens, min_seconds=0.0):
+    """Oracle on the first ``sample_tokens`` tokens of every sequence x all heads,
+    repeated until ``min_seconds`` of wall time have passed (at least once)."""
     from oracle import gdn_recurrence_f64
-    sl = (slice(0, 1), slice(0, sample_tokens))
+    sl = (slice(None), slice(0, sample_tokens))
     cores = os.cpu_count() or 1
     args = [x[k][sl] for k in ("q", "k", "v", "log_alpha", "beta")]
-    t0 = time.perf_counter()
-    gdn_recurrence_f64(*args, n_threads=cores)
-    dt = time.perf_counter() - t0
-    return dict(value=sample_tokens / dt, unit="tokens/s", cores=min(cores, w.H), kind="oracle",
-                sample="1 of %d sequences x %d heads x first %d of %d tokens (%s), fp64, "
-                       "%.2f s" % (w.B, w.H, sample_tokens, w.T, w.name, dt))
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        gdn_recurrence_f64(*args, n_threads=cores)
+        reps += 1
+        dt = time.perf_counter() - t0
+        if dt >= min_seconds:
+            break
+    tokens = reps * w.B * sample_tokens
+    return dict(value=tokens / dt, unit="tokens/s", cores=min(cores, w.B * w.H), kind="oracle",
+                sample="%d x (%d sequences x %d heads x first %d of %d tokens) of %s, fp64, "
+                       "%.2f s" % (reps, w.B, w.H, sample_tokens, w.T, w.name, dt))
 
 
 def run_reference(args, world, rank):
@@ -218,16 +224,16 @@ def run_reference(args, world, rank):
     times = []
     for _ in range(args.steps):
         cb = cpu_baseline(w, x, sample)
-        times.append(sample / cb["value"])
+        times.append(w.B * sample / cb["value"])
     total = sum(times)
-    value = args.steps * sample / total
+    value = args.steps * w.B * sample / total
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": "%s: B%d H%d T%d d_k=%d d_v=%d C%d, each step a sample "
-                                   "of %d tokens x %d heads" % (w.name, w.B, w.H, w.T, w.dk,
-                                                                w.dv, w.C, sample, w.H)},
+            "config": {"workload": "%s: B%d H%d T%d d_k=%d d_v=%d C%d, each step the oracle "
+                                   "on the first %d tokens of each sequence, all heads"
+                                   % (w.name, w.B, w.H, w.T, w.dk, w.dv, w.C, sample)},
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cb["cores"],
                              "kind": "oracle", "sample": cb["sample"]},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
@@ -339,7 +345,7 @@ def run_ours(args, world, rank, local):
     gbs = byts / kernel_s / 1e9
     tflops = flops / (ms * 1e-3) / 1e12
     value = world * tokens / (ms_max * 1e-3)
-    cb = (cpu_baseline(w, x, min(args.cpu_tokens, w.T or tokens))
+    cb = (cpu_baseline(w, x, min(args.cpu_tokens, w.T or tokens), args.cpu_seconds)
           if (world == 1 and not args.no_cpu_baseline) else None)
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
@@ -378,10 +384,12 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--e2e-steps", type=int, default=50)
-    ap.add_argument("--ref-tokens", type=int, default=512,
-                    help="tokens per oracle sample (one sequence, all heads)")
+    ap.add_argument("--ref-tokens", type=int, default=256,
+                    help="tokens of each sequence per oracle step (all sequences, all heads)")
     ap.add_argument("--cpu-tokens", type=int, default=4096,
-                    help="tokens of the oracle sample for the cpu_baseline key")
+                    help="tokens of each sequence in the oracle sample for the cpu_baseline key")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="the cpu_baseline sample repeats until this much wall time has passed")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     world, rank, local = dist_setup()
