@@ -376,12 +376,148 @@ def run_ours(args, world, rank, local):
     print(json.dumps(line), flush=True)
 
 
+DECODE_METRIC = "GDN decode-step tokens/s and % of HBM bandwidth (N256 H16 d128, fp32 state in place)"
+
+
+def decode_numbers(N, H, T, dk, dv, esz):
+    """Algorithmic bytes and FLOPs of one decode call: the fp32 state read and
+    written once, q, k, v read and o written once, 8 B of gates per
+    token-head; per token-head 2 d_k d_v FLOP for each of r = S k, the rank-1
+    update and o = S q, plus d_k d_v for the decay."""
+    byts = 2 * N * H * dv * dk * 4 + N * T * H * ((2 * dk + 2 * dv) * esz + 8)
+    flops = N * T * H * 7 * dk * dv
+    return flops, byts
+
+
+def run_decode(args, world, rank, local):
+    import torch
+    import gated_delta_rule_09_gb300 as gdn
+    from gated_delta_rule_09_gb300 import inputs as I
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    x = I.decode_inputs(seed=rank)
+    N, T, H, dk = x["q"].shape
+    dv = x["v"].shape[-1]
+    esz = x["q"].element_size()
+    flops, byts = decode_numbers(N, H, T, dk, dv, esz)
+    keys = ("q", "k", "v", "log_alpha", "beta")
+    d = {kk: x[kk].to(dev) for kk in keys}
+    S = x["S0"].to(dev)                     # the cache, updated in place every step
+    o = torch.empty(x["v"].shape, dtype=x["v"].dtype, device=dev)
+    stream = torch.cuda.Stream(dev)
+
+    def step():
+        gdn.gdn_decode_step(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], S_in=S, o=o,
+                            S_out=S, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(args.warmup, 3)):
+            step()
+    torch.cuda.synchronize(dev)
+    assert gdn.gdn_get_device_status(stream) == 0
+    launches_per_step, path = gdn.gdn_last_launch_count()
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    t_start = time.time()
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    t_end = time.time()
+    barrier(world)
+    rows = sampler.stop()
+    ms = ev0.elapsed_time(ev1) / args.steps
+    ms_max = max_over_ranks(ms, world)
+    clocks = ClockSampler.summarise(rows, t_start, t_end)
+
+    # end to end: the step's token inputs from pinned host memory, the call,
+    # its outputs back to pinned host memory; the state is the device-resident
+    # cache and does not move
+    host = {kk: x[kk].pin_memory() for kk in keys}
+    out_o = torch.empty(x["v"].shape, dtype=x["v"].dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_o.numel() * out_o.element_size()
+    e2e_steps = max(1, min(args.steps, args.e2e_steps))
+
+    def e2e_step():
+        for kk in keys:
+            d[kk].copy_(host[kk], non_blocking=True)
+        step()
+        out_o.copy_(o, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world)
+    barrier(world)
+    if rank != 0:
+        return
+    peaks, peak_src = load_peaks()
+    gbs = byts / (ms * 1e-3) / 1e9
+    tokens = N * T
+    cb = None
+    if world == 1 and not args.no_cpu_baseline:
+        from oracle import gdn_recurrence_f64
+        cores = os.cpu_count() or 1
+        reps, t0 = 0, time.perf_counter()
+        while True:
+            gdn_recurrence_f64(*[x[kk] for kk in keys], S0=x["S0"], n_threads=cores)
+            reps += 1
+            dt = time.perf_counter() - t0
+            if dt >= args.cpu_seconds:
+                break
+        cb = {"value": reps * tokens / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+              "sample": "%d x the whole decode batch (%d sequences x %d heads x %d token), "
+                        "fp64, %.2f s" % (reps, N, H, T, dt)}
+    line = {
+        "metric": DECODE_METRIC, "value": world * tokens / (ms_max * 1e-3), "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": "decode_bf16: N%d H%d T%d d_k=%d d_v=%d, bf16 q/k/v/o, fp32 "
+                               "state updated in place" % (N, H, T, dk, dv),
+                   "tokens_per_step": tokens,
+                   "l2": "inputs larger than L2 (%.0f MB of state read and written per step "
+                         "vs %.0f MB L2)" % (byts / 1e6, L2_BYTES / 1e6),
+                   "parallelism": "replicas x%d" % world, "kernel_path": "recurrent decode"},
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": gbs / peaks["hbm_gbs"], "traffic": recorded_traffic("decode_bf16"),
+                     "algorithmic_bytes": byts, "peak_source": peak_src,
+                     "algorithmic_flops": flops},
+        "clocks": clocks,
+        "e2e": {"value": world * tokens / (e2e_ms * 1e-3), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": launches_per_step * args.steps,
+        "cpu_baseline": cb,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--op", choices=["chunk", "decode"], default="chunk",
+                    help="chunk: the chunkwise forward (default); decode: the recurrent "
+                         "decode step on the decode batch")
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--ref-tokens", type=int, default=256,
@@ -395,6 +531,8 @@ def main(argv=None):
     world, rank, local = dist_setup()
     if args.impl == "reference":
         run_reference(args, world, rank)
+    elif args.op == "decode":
+        run_decode(args, world, rank, local)
     else:
         run_ours(args, world, rank, local)
     if world > 1:

@@ -92,6 +92,59 @@ def gdn_chunk_fwd(q, k, v, log_alpha, beta, S0=None, o=None, S_final=None,
     return o, S_final
 
 
+def _stream_handle(stream, device):
+    if stream is None:
+        return torch.cuda.current_stream(device).cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def gdn_decode_step(q, k, v, log_alpha, beta, S_in=None, o=None, S_out=None, stream=None):
+    """Recurrent (token-by-token) gated delta rule; returns ``(o, S_out)``.
+
+    q, k [N,T,H,d_k] and v [N,T,H,d_v] (fp32 or bf16, one dtype), or
+    [N,H,d] for a single token; log_alpha, beta [N,T,H] (or [N,H]) fp32;
+    S_in [N,H,d_v,d_k] fp32 or None (zeros).  ``S_out`` may be ``S_in`` for an
+    in-place update; if None a new tensor is allocated.
+    """
+    lib = _lib.load()
+    if q.dtype not in _DTYPES:
+        raise TypeError("q/k/v dtype must be float32 or bfloat16, got %s" % q.dtype)
+    single = q.dim() == 3
+    if single:
+        q, k, v = q.unsqueeze(1), k.unsqueeze(1), v.unsqueeze(1)
+        log_alpha, beta = log_alpha.unsqueeze(1), beta.unsqueeze(1)
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _need_cuda(name, t, q.dtype)
+    _need_cuda("log_alpha", log_alpha, torch.float32)
+    _need_cuda("beta", beta, torch.float32)
+    _need_cuda("S_in", S_in, torch.float32)
+    if q.dim() != 4 or k.shape != q.shape or v.dim() != 4 or v.shape[:3] != q.shape[:3]:
+        raise ValueError("q, k must be [N,T,H,d_k] and v [N,T,H,d_v]")
+    N, T, H, dk = q.shape
+    dv = v.shape[-1]
+    if log_alpha.shape != (N, T, H) or beta.shape != (N, T, H):
+        raise ValueError("log_alpha and beta must be [N,T,H]")
+    if S_in is not None and S_in.shape != (N, H, dv, dk):
+        raise ValueError("S_in must be [N,H,d_v,d_k] = %s" % ((N, H, dv, dk),))
+    if o is None:
+        o = torch.empty((N, T, H, dv), dtype=q.dtype, device=q.device)
+    elif single:
+        o = o.unsqueeze(1)
+    _need_cuda("o", o, q.dtype)
+    if S_out is None:
+        S_out = torch.empty((N, H, dv, dk), dtype=torch.float32, device=q.device)
+    _need_cuda("S_out", S_out, torch.float32)
+    with torch.cuda.device(q.device):
+        st = lib.gdn_decode_step(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(S_in),
+            _ptr(o), _ptr(S_out), N, H, T, dk, dv, _DTYPES[q.dtype],
+            ctypes.c_void_p(_stream_handle(stream, q.device)))
+    _lib.check(st)
+    return (o.squeeze(1) if single else o), S_out
+
+
 def gdn_get_device_status(stream=None):
     """Synchronise and return (then clear) the device status bits."""
     handle = (torch.cuda.current_stream().cuda_stream if stream is None
@@ -102,7 +155,8 @@ def gdn_get_device_status(stream=None):
 
 
 def gdn_last_launch_count():
-    """(kernels enqueued by the last gdn_chunk_fwd on this thread, path id)."""
+    """(kernels enqueued by the last gdn_chunk_fwd / gdn_decode_step on this
+    thread, path id: 0 fp32 chunk kernel, 1 tcgen05 chunk kernel, 2 decode)."""
     path = ctypes.c_int(-1)
     n = _lib.load().gdn_last_launch_count(ctypes.byref(path))
     return n, path.value

@@ -165,4 +165,63 @@ gdn_status_t gdn_chunk_fwd(const void *q, const void *k, const void *v,
     return GDN_OK;
 }
 
+gdn_status_t gdn_decode_step(const void *q, const void *k, const void *v,
+                             const float *log_alpha, const float *beta,
+                             const float *S_in, void *o, float *S_out,
+                             int N, int H, int T, int d_k, int d_v,
+                             gdn_dtype_t dtype, void *stream)
+{
+    t_msg[0] = '\0';
+    if (N < 0 || H < 0 || T < 0)
+        return fail(GDN_ERR_INVALID_ARG, "negative size: N=%d H=%d T=%d", N, H, T);
+    if (d_k < 1 || d_v < 1)
+        return fail(GDN_ERR_INVALID_ARG, "head dims must be >= 1: d_k=%d d_v=%d", d_k, d_v);
+    if (dtype != GDN_F32 && dtype != GDN_BF16)
+        return fail(GDN_ERR_UNSUPPORTED, "dtype %d (expected GDN_F32 or GDN_BF16)", (int)dtype);
+    if (d_k > 128)
+        return fail(GDN_ERR_UNSUPPORTED, "d_k=%d (supported: 1..128)", d_k);
+
+    const size_t esz = dtype == GDN_BF16 ? 2 : 4;
+    const size_t tokens = (size_t)N * T;
+    const size_t nqk = tokens * H * d_k * esz, nv = tokens * H * d_v * esz;
+    const size_t ng = tokens * H * sizeof(float);
+    const size_t ns = (size_t)N * H * d_v * d_k * sizeof(float);
+    const bool any_units = (size_t)N * H > 0;
+    const bool work = any_units && T > 0;
+
+    if (any_units && !S_out) return fail(GDN_ERR_INVALID_ARG, "S_out must be non-NULL");
+    if (work && (!q || !k || !v || !log_alpha || !beta || !o))
+        return fail(GDN_ERR_INVALID_ARG, "q, k, v, log_alpha, beta and o must be non-NULL");
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16))
+        return fail(GDN_ERR_INVALID_ARG, "q, k, v and o must be 16-byte aligned");
+    if (!aligned(log_alpha, 4) || !aligned(beta, 4) || !aligned(S_in, 4) || !aligned(S_out, 4))
+        return fail(GDN_ERR_INVALID_ARG, "log_alpha, beta, S_in and S_out must be 4-byte aligned");
+    if (work && (overlaps(o, nv, q, nqk) || overlaps(o, nv, k, nqk) || overlaps(o, nv, v, nv) ||
+                 overlaps(o, nv, log_alpha, ng) || overlaps(o, nv, beta, ng) ||
+                 overlaps(o, nv, S_in, ns) || overlaps(o, nv, S_out, ns)))
+        return fail(GDN_ERR_INVALID_ARG, "o overlaps another argument");
+    if (S_out != S_in &&
+        (overlaps(S_out, ns, q, nqk) || overlaps(S_out, ns, k, nqk) || overlaps(S_out, ns, v, nv) ||
+         overlaps(S_out, ns, log_alpha, ng) || overlaps(S_out, ns, beta, ng) ||
+         overlaps(S_out, ns, S_in, ns)))
+        return fail(GDN_ERR_INVALID_ARG, "S_out overlaps an input (only S_out == S_in is allowed)");
+
+    t_launches = 0;
+    t_path = -1;
+    if (!any_units) return GDN_OK;
+
+    GdnDecodeArgs a;
+    a.q = q; a.k = k; a.v = v; a.log_alpha = log_alpha; a.beta = beta;
+    a.S_in = S_in; a.o = o; a.S_out = S_out;
+    a.N = N; a.H = H; a.T = T; a.dk = d_k; a.dv = d_v;
+    a.dtype = dtype == GDN_BF16 ? 1 : 0;
+    int launches = 0;
+    cudaError_t e = gdn_launch_decode(a, static_cast<cudaStream_t>(stream), &launches);
+    if (e != cudaSuccess)
+        return fail(GDN_ERR_CUDA, "kernel launch (decode): %s", cudaGetErrorString(e));
+    t_launches = launches;
+    t_path = 2;
+    return GDN_OK;
+}
+
 }  // extern "C"

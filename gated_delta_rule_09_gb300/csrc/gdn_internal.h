@@ -24,3 +24,17 @@ size_t gdn_simt_smem_bytes(int C, int dk);
 // tcgen05 tensor-core kernel: bf16, the shapes gdn_tc_supported() accepts.
 bool gdn_tc_supported(const GdnArgs &a);
 cudaError_t gdn_launch_tc(const GdnArgs &a, cudaStream_t s, int *launches);
+
+struct GdnDecodeArgs {
+    const void *q, *k, *v;       // [N, T, H, dk] / [N, T, H, dv], dtype
+    const float *log_alpha;      // [N, T, H]
+    const float *beta;           // [N, T, H]
+    const float *S_in;           // [N, H, dv, dk] or null (zeros)
+    void *o;                     // [N, T, H, dv], dtype
+    float *S_out;                // [N, H, dv, dk]; may equal S_in
+    int N, H, T, dk, dv;
+    int dtype;                   // 0 = fp32, 1 = bf16
+};
+
+// Recurrent (token-by-token) kernel for decoding, on CUDA cores.
+cudaError_t gdn_launch_decode(const GdnDecodeArgs &a, cudaStream_t s, int *launches);

@@ -26,6 +26,10 @@ The five named workloads:
                     k ~ N(0,1) then unit norm; beta ~ U(0,1); q,v ~ N(0,1);
                     S0 ~ N(0, sd 0.02).
 ==================  ==========================================================
+
+The decode batch (``decode_inputs``): 256 sequences x 16 heads, d_k = d_v =
+128, bf16, one token each from a state S_in ~ N(0, sd 0.02), with the
+``small_bf16`` distributions for q, k, v, beta and log alpha.
 """
 from __future__ import annotations
 
@@ -149,3 +153,10 @@ def custom(B, H, T, dk, dv, C, dtype="bf16", seed=0, lengths=None,
     w = Workload("custom", B if lengths is None else len(lengths), H, T, dk, dv,
                  C, dtype, q_unit, beta, alpha, s0, varlen=lengths is not None)
     return generate(w, seed=seed, lengths=lengths)
+
+
+def decode_inputs(seed=0, N=256, H=16, T=1, dk=128, dv=128, dtype="bf16"):
+    """The decode batch: ``N`` sequences x ``H`` heads advancing ``T`` tokens
+    from a state S_in ~ N(0, sd 0.02) (returned as ``S0``); the other tensors
+    as ``custom`` draws them, laid out [N, T, H, *]."""
+    return custom(N, H, T, dk, dv, 64, dtype=dtype, seed=seed, s0="normal_0.02")

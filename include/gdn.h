@@ -112,6 +112,49 @@ gdn_status_t gdn_chunk_fwd(const void *q, const void *k, const void *v,
                            void *stream);
 
 /*
+ * gdn_decode_step — the same recurrence evaluated token by token, for decoding
+ * ("从零开始的 GDN 推导", recurrent form of the gated delta rule;
+ * "RNN的复兴03：现代RNN的并行计算", §一, delta-rule update), batched over
+ * (sequence, head).  Per token, with r = S k:
+ *
+ *     S <- alpha S + beta (v - alpha r) k^T      o = S q
+ *
+ * which is the spec update alpha S (I - beta k k^T) + beta v k^T
+ * rearranged.  T is the number of tokens each sequence advances in this call
+ * (1 for one decoding step); the state stays on chip between them.  The
+ * state written by gdn_chunk_fwd (S_final) is the state this call reads, so a
+ * prefill with gdn_chunk_fwd followed by decode steps reproduces the
+ * recurrence over the whole sequence.
+ *
+ * Arguments:
+ *   q, k       [N, T, H, d_k]  dtype   queries, keys
+ *   v          [N, T, H, d_v]  dtype   values
+ *   log_alpha  [N, T, H]       fp32    log of the decay gate
+ *   beta       [N, T, H]       fp32    write strength (any real value)
+ *   S_in       [N, H, d_v, d_k] fp32   state before the first token, or NULL
+ *                                      for zeros
+ *   o          [N, T, H, d_v]  dtype   outputs; must not overlap anything
+ *   S_out      [N, H, d_v, d_k] fp32   state after the last token (required);
+ *                                      may be exactly S_in (in-place update),
+ *                                      must not overlap anything else.  With
+ *                                      T = 0 it receives S_in (or zeros).
+ *   N, H, T, d_k, d_v  sizes; d_k in [1, 128], d_v >= 1
+ *   dtype      GDN_F32 or GDN_BF16 (q, k, v and o share it); arithmetic is
+ *              fp32 on CUDA cores either way
+ *   stream     cudaStream_t to enqueue on
+ *
+ * Alignment: q, k, v, o 16 bytes; log_alpha, beta, S_in, S_out 4 bytes
+ * (16 bytes and d_k a multiple of 4 select the vectorised kernel).
+ * Returns GDN_OK once the work is enqueued (one kernel; gdn_last_launch_count
+ * reports path 2), or an error status with nothing enqueued.
+ */
+gdn_status_t gdn_decode_step(const void *q, const void *k, const void *v,
+                             const float *log_alpha, const float *beta,
+                             const float *S_in, void *o, float *S_out,
+                             int N, int H, int T, int d_k, int d_v,
+                             gdn_dtype_t dtype, void *stream);
+
+/*
  * gdn_get_device_status — synchronise `stream`, then read and clear the
  * device-side status bits (GDN_DEV_*) raised by kernels of this library on the
  * current device since the last read.  *flags receives the bits (0 = clean).
@@ -127,8 +170,9 @@ int gdn_version(void);
 
 /*
  * gdn_last_launch_count — number of kernels the last successful gdn_chunk_fwd
- * on the calling thread enqueued, and in *path which kernel family ran
- * (0 = fp32 CUDA-core kernel, 1 = tcgen05 tensor-core kernel).  For
+ * or gdn_decode_step on the calling thread enqueued, and in *path which
+ * kernel family ran (0 = fp32 CUDA-core chunk kernel, 1 = tcgen05
+ * tensor-core chunk kernel, 2 = recurrent decode kernel).  For
  * accounting in benchmarks; no device work.
  */
 int gdn_last_launch_count(int *path);

@@ -90,3 +90,28 @@ def test_python_binding_rejects_cpu_tensors():
     x = torch.zeros(1, 4, 1, 16)
     with pytest.raises(TypeError):
         gdn.gdn_chunk_fwd(x, x, x, torch.zeros(1, 4, 1), torch.zeros(1, 4, 1))
+
+
+def _dcall(lib, q=0x1000, k=0x100000, v=0x200000, la=0x300000, be=0x400000, Si=None,
+           o=0x500000, So=0x600000, N=1, H=1, T=1, dk=16, dv=16, dtype=1):
+    return lib.gdn_decode_step(q, k, v, la, be, Si, o, So, N, H, T, dk, dv, dtype, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(dtype=3), 2), (dict(dk=129), 2),
+    (dict(N=-1), 1), (dict(T=-1), 1), (dict(dk=0), 1), (dict(dv=0), 1),
+    (dict(So=None), 1), (dict(q=None), 1), (dict(o=None), 1), (dict(be=None), 1),
+    (dict(k=0x100004), 1), (dict(So=0x600002), 1),
+    (dict(o=0x200000), 1),                     # o aliases v
+    (dict(So=0x400000), 1),                    # S_out overlaps beta
+    (dict(Si=0x700000, So=0x700010), 1),       # partial overlap of S_in / S_out
+])
+def test_decode_host_validation(lib, kw, code):
+    st = _dcall(lib, **kw)
+    assert st == code, (kw, st, lib.gdn_get_last_error())
+    assert lib.gdn_get_last_error()
+
+
+def test_decode_empty_problem_is_a_no_op(lib):
+    assert _dcall(lib, N=0) == 0
+    assert _dcall(lib, H=0, So=None) == 0
