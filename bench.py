@@ -70,25 +70,29 @@ def workload_numbers(w, lengths):
     return flops, byts
 
 
-def kernel_source_sha():
+# Source files whose code each recorded traffic figure was measured on.
+KERNEL_SOURCES = {"train_bf16": ("gdn_tc.cu", "sm100_ptx.cuh"),
+                  "decode_bf16": ("gdn_decode.cu",)}
+
+
+def kernel_source_sha(workload="train_bf16"):
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "gated_delta_rule_09_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".h", ".cuh")):
-            with open(os.path.join(csrc, name), "rb") as fh:
-                h.update(fh.read())
+    for name in sorted(KERNEL_SOURCES.get(workload, ())):
+        with open(os.path.join(csrc, name), "rb") as fh:
+            h.update(fh.read())
     return h.hexdigest()[:16]
 
 
 def recorded_traffic(workload):
     """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the kernel sources as they are now (else None)."""
+    on the kernel's sources as they are now (else None)."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
     try:
         text = open(path).read()
     except OSError:
         return None
-    sha = kernel_source_sha()
+    sha = kernel_source_sha(workload)
     for line in text.splitlines():
         m = re.match(r"\s*(\w+)\s+sha=(\w+)\s+dram_bytes_per_launch=(\d+)", line)
         if m and m.group(1) == workload and m.group(2) == sha:
