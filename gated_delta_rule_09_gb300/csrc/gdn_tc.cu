@@ -1,42 +1,47 @@
 // tcgen05 tensor-core kernel for the chunkwise gated delta rule (bf16 in/out,
 // fp32 state and accumulation, fp16 tensor-core operands) on sm_103a.
 //
-// Work unit: one (sequence, head, 128-wide d_v tile), walked chunk by chunk
-// (C = 64 tokens).  In the notation of "从零开始的 GDN 推导" (§"UT transform",
-// §"S 的推导", §"O 的推导", §"总结"), transposed so that S is d_v x d_k, with
-// g the in-chunk cumulative sum of log alpha:
+// Work unit: one (sequence, head, 128-row d_v tile), walked chunk by chunk
+// (C = 64 tokens).  d_k up to 128 and d_v a multiple of 8: the TMA loads
+// zero-fill features past d_k and rows past d_v, so every tile is 128 wide
+// and the padding contributes exact zeros.  In the notation of "从零开始的
+// GDN 推导" (§"UT transform", §"S 的推导", §"O 的推导", §"总结"), transposed so
+// that S is d_v x d_k, with g the in-chunk cumulative sum of log alpha:
 //
 //   state-independent:  A = StrictLower(diag(beta) K K^T * e^{g_i-g_j})
 //                       P = Lower(Q K^T * e^{g_i-g_j})
 //                       T = (I + A)^{-1}
-//                       W = T diag(beta e^g) K,   T' = T diag(beta)
-//   state chain:        U^T = V^T T'^T,   V_new^T = U^T - S W^T
+//                       T'' = T diag(beta e^g),   T' = T diag(beta)
+//                       W^T = K^T T''^T,          U^T = V^T T'^T
+//   state chain:        V_new^T = U^T - S W^T
 //                       O^T = e^{g} (S Q^T) + V_new^T P^T
 //                       S <- e^{g_C} S + (V_new * e^{g_C - g})^T K
 //
 // Each unit runs on a cluster of two CTAs on two SMs:
 //
-//  * rank 0, the producer, computes the state-independent part of every chunk
-//    with two 4-warp pipelines (even and odd chunks): TMA loads of the q/k
-//    tiles, [K;Q] K^T on the tensor cores, A and P on the CUDA cores, the
-//    blocked inverse, W^T = K^T (T diag(beta e^g))^T on the tensor cores, and
-//    ships W, P, T' and the decay vectors into the consumer's ring slot with
-//    one distributed-shared-memory bulk copy that completes on the consumer's
-//    mbarrier.
+//  * rank 0, the producer, computes A, P, T, T' and T'' for every chunk with
+//    two 4-warp pipelines (even and odd chunks): TMA loads of the q/k tiles,
+//    [K;Q] K^T on the tensor cores, A and P on the CUDA cores, the blocked
+//    inverse, and ships P, T', T'' and the decay vectors (25 KB) into the
+//    consumer's ring slot with one distributed-shared-memory bulk copy that
+//    completes on the consumer's mbarrier.
 //  * rank 1, the consumer, keeps the state slice (128 x 128 fp32) in TMEM for
-//    the whole walk.  Warps 0-3 run the state chain (fp16 copy of S, then
-//    V^T T'^T, S W^T and S Q^T, V_new, then V_new^T P^T and the state update);
-//    warps 4-7 convert the next chunk's q/k/v tiles (the consumer's own TMA
-//    loads) and write the previous chunk's outputs from double-buffered TMEM.
+//    the whole walk and loads its own q/k/v tiles by TMA.  Warps 0-3 run the
+//    state chain (fp16 copy of S, S W^T and S Q^T, V_new, V_new^T P^T and the
+//    state update) and issue the next chunk's W^T and U^T one chunk ahead;
+//    warps 4-7 convert the q/k/v tiles to fp16 and read W^T out of TMEM into
+//    its operand tile; warps 8-11 write the outputs (TMA bulk tensor stores
+//    for full chunks).
 //
 // Every MMA has M = 128, so a result row is one TMEM lane and one epilogue
 // thread.  Operands are fp16 (11-bit significand; bf16 operands would leave
 // about 0.03 x RMS of error in o on the bf16 workloads, fp16 about 0.003):
-// the bf16 q/k/v tiles are converted in shared memory (exact for |x| < 65504)
-// and every epilogue-written operand is fp16; accumulation and the state are
-// fp32.  Values outside the fp16 range raise GDN_DEV_F16_RANGE.  Every wait is
-// bounded: on timeout the CTA raises GDN_DEV_WAIT_TIMEOUT and stops waiting,
-// so the kernel always finishes.
+// the bf16 q/k/v tiles are converted in shared memory (exact for normal fp16
+// magnitudes, |x| in [2^-14, 65504]) and every epilogue-written operand is
+// fp16; K K^T and Q K^T keep bf16 operands (exact products).  Accumulation
+// and the state are fp32.  Values outside the fp16 range raise
+// GDN_DEV_F16_RANGE.  Every wait is bounded: on timeout the CTA raises
+// GDN_DEV_WAIT_TIMEOUT and stops waiting, so the kernel always finishes.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -52,8 +57,8 @@ namespace {
 using namespace sm100;
 
 constexpr int kC = 64;       // chunk length
-constexpr int kDK = 128;     // d_k
-constexpr int kDVT = 128;    // d_v columns per unit
+constexpr int kDK = 128;     // d_k as the tiles hold it (a smaller d_k is zero-padded)
+constexpr int kDVT = 128;    // d_v rows per unit (rows past d_v are zero padding)
 constexpr int kThreads = 384;  // producer: 2 x 4 warps (warps 8-11 idle); consumer: 3 x 4 warps
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
 constexpr float kF16Max = 65504.f;
@@ -571,12 +576,14 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
             if (nchunks > 0) issue_qkv(0);
             if (nchunks > 1) issue_qkv(1);
         }
-        {   // initial state -> TMEM
-            const float *src = a.S0 ? a.S0 + (((size_t)n * H + h) * dv + v0 + t) * kDK : nullptr;
+        {   // initial state -> TMEM; padding rows and columns stay zero
+            const int dk = a.dk;
+            const float *src = a.S0 && v0 + t < dv ? a.S0 + (((size_t)n * H + h) * dv + v0 + t) * dk
+                                                   : nullptr;
             for (int cb = 0; cb < 4; ++cb) {
                 float x[32];
 #pragma unroll
-                for (int j = 0; j < 32; ++j) x[j] = src ? src[cb * 32 + j] : 0.f;
+                for (int j = 0; j < 32; ++j) x[j] = src && cb * 32 + j < dk ? src[cb * 32 + j] : 0.f;
                 tmem_st32(lane_addr(tbase, quad, kColS + cb * 32), x);
             }
             tmem_st_wait();
@@ -731,14 +738,23 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
                 }
             }
         }
-        if (a.S_final && !*abort_flag) {
-            float *dst = a.S_final + (((size_t)n * H + h) * dv + v0 + t) * kDK;
-            for (int cb = 0; cb < 4; ++cb) {
+        // one reading of the abort flag per warp keeps the branch warp-uniform
+        const bool aborted = __shfl_sync(0xffffffffu, *abort_flag, 0) != 0;
+        if (a.S_final && !aborted) {
+            // every lane takes part in the (warp-collective) TMEM loads; only
+            // rows below d_v and columns below d_k are stored
+            const int dk = a.dk;
+            const bool row_ok = v0 + t < dv;
+            float *dst = a.S_final + (((size_t)n * H + h) * dv + (row_ok ? v0 + t : 0)) * dk;
+            for (int cb = 0; cb < 4 && cb * 32 < dk; ++cb) {
                 float x[32];
                 tmem_ld32(lane_addr(tbase, quad, kColS + cb * 32), x);
                 tmem_ld_wait();
+                if (row_ok) {
 #pragma unroll
-                for (int j = 0; j < 32; ++j) dst[cb * 32 + j] = x[j];
+                    for (int j = 0; j < 32; ++j)
+                        if (cb * 32 + j < dk) dst[cb * 32 + j] = x[j];
+                }
             }
         }
     } else {
@@ -786,7 +802,7 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
                         reinterpret_cast<__nv_bfloat16 *>(stage + sw128(i, vc))[ve] =
                             __float2bfloat16_rn(fmaf(s->egc[sl][i], x[j], y[j]));
                     }
-                } else {
+                } else if (col < (size_t)dv) {
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
                         const int i = half * 32 + j;
@@ -801,9 +817,9 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
             if (nc == kC) {
                 fence_async_smem();
                 named_sync(3, 128);
-                if (t == 0) {
+                if (t == 0) {  // the store clips columns past d_v; a box wholly past it is skipped
                     tma_store_3d(tm_o, slot + kOutP, v0, h, (int)tok0);
-                    tma_store_3d(tm_o, slot + kOutP + 8192, v0 + 64, h, (int)tok0);
+                    if (v0 + 64 < dv) tma_store_3d(tm_o, slot + kOutP + 8192, v0 + 64, h, (int)tok0);
                     bulk_commit();
                     bulk_wait_read();
                 }
@@ -962,7 +978,9 @@ bool make_map(CUtensorMap *m, const void *base, long tokens, int H, int d)
 bool gdn_tc_supported(const GdnArgs &a)
 {
     const long tokens = a.cu_seqlens ? (long)a.T : (long)a.N * a.T;
-    return a.dtype == 1 && a.dk == kDK && a.dv % kDVT == 0 && a.C == kC && tokens > 0 &&
+    // d_k and d_v multiples of 8 keep every TMA row stride a multiple of 16
+    // bytes; features past d_k and rows past d_v are zero-filled by the loads
+    return a.dtype == 1 && a.dk % 8 == 0 && a.dk <= kDK && a.dv % 8 == 0 && a.C == kC && tokens > 0 &&
            tokens < (1L << 31) && encoder() != nullptr;
 }
 
@@ -976,7 +994,7 @@ cudaError_t gdn_launch_tc(const GdnArgs &a, cudaStream_t s, int *launches)
     cudaError_t e = cudaFuncSetAttribute(gdn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          kSmemBytes);
     if (e != cudaSuccess) return e;
-    dim3 grid(2 * (a.dv / kDVT), a.H, a.N);
+    dim3 grid(2 * ((a.dv + kDVT - 1) / kDVT), a.H, a.N);
     gdn_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(a, mq, mk, mv, mo);
     *launches = 1;
     return cudaGetLastError();

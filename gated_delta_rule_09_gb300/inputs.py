@@ -8,7 +8,7 @@ in fp64 where a workload asks for unit-norm keys or queries, then rounded once
 to the workload's dtype (round-to-nearest-even for bf16).  The oracle sees the
 same rounded values widened back to fp64.
 
-The five named workloads:
+The named workloads:
 
 ==================  ==========================================================
 ``tiny_f32``        B1 H1 T64 d_k=d_v=16 C16, fp32.  q,v ~ N(0,1); k ~ N(0,1)
@@ -25,6 +25,9 @@ The five named workloads:
 ``wide_ungated_bf16`` B8 H8 T2048 d_k128 d_v256 C64; alpha == 1 (log alpha 0);
                     k ~ N(0,1) then unit norm; beta ~ U(0,1); q,v ~ N(0,1);
                     S0 ~ N(0, sd 0.02).
+``hybrid_bf16``     B4 H16 T4096 d_k96 d_v192 C64 (the hybrid model's head
+                    shape); beta ~ U(0,2) (the extended range); otherwise the
+                    ``small_bf16`` distributions; no S0.
 ==================  ==========================================================
 
 The decode batch (``decode_inputs``): 256 sequences x 16 heads, d_k = d_v =
@@ -51,7 +54,7 @@ class Workload:
     C: int
     dtype: str             # "f32" or "bf16"
     q_unit: bool           # normalise q per token
-    beta_dist: str         # "uniform" | "sigmoid_normal"
+    beta_dist: str         # "uniform" | "uniform_0_2" | "sigmoid_normal"
     alpha_dist: str        # "uniform_0.9_1" | "softplus_0.1" | "one"
     s0: str                # "none" | "zeros" | "normal_0.02"
     varlen: bool = False
@@ -71,6 +74,8 @@ WORKLOADS = {
                             varlen=True, len_lo=1024, len_hi=8192),
     "wide_ungated_bf16": Workload("wide_ungated_bf16", 8, 8, 2048, 128, 256, 64,
                                   "bf16", False, "uniform", "one", "normal_0.02"),
+    "hybrid_bf16": Workload("hybrid_bf16", 4, 16, 4096, 96, 192, 64, "bf16", True,
+                            "uniform_0_2", "softplus_0.1", "none"),
 }
 
 TORCH_DTYPE = {"f32": torch.float32, "bf16": torch.bfloat16}
@@ -118,6 +123,8 @@ def generate(w: Workload, seed: int = 0, lengths=None, S0: Optional[str] = None)
     v = rng.standard_normal((Bt, Tt, H, dv))
     if w.beta_dist == "uniform":
         beta = rng.uniform(0.0, 1.0, (Bt, Tt, H))
+    elif w.beta_dist == "uniform_0_2":
+        beta = rng.uniform(0.0, 2.0, (Bt, Tt, H))
     else:
         beta = _sigmoid(rng.standard_normal((Bt, Tt, H)))
     if w.alpha_dist == "uniform_0.9_1":

@@ -95,9 +95,9 @@ typedef enum { GDN_F32 = 0, GDN_BF16 = 1 } gdn_dtype_t;
  * Alignment: q, k, v, o must be aligned to 16 bytes; log_alpha, beta, S0 and
  * S_final to 4 bytes (16 bytes lets the fastest path run).
  * Supported shapes: d_k in [1, 128], d_v >= 1, C in {16, 32, 64}.  The
- * tcgen05 tensor-core kernel serves bf16 with d_k = 128, d_v a multiple of
- * 128 and C = 64; every other supported shape runs on the fp32 CUDA-core
- * kernel (gdn_last_launch_count reports which ran).  Both are CUDA kernels
+ * tcgen05 tensor-core kernel serves bf16 with C = 64 and d_k, d_v multiples
+ * of 8 (tiles zero-padded to 128); every other supported shape runs on the
+ * fp32 CUDA-core kernel (gdn_last_launch_count reports which ran).  Both are CUDA kernels
  * of this library.
  *
  * Returns GDN_OK once the work is enqueued, or an error status (nothing

@@ -52,11 +52,30 @@ def test_ragged_lengths(gdn, dtype, T, C):
     run_and_check(gdn, x, C, dtype)
 
 
+def tc_path_expected(dk, dv, C, dtype):
+    """The tcgen05 kernel takes bf16, C = 64, d_k <= 128 and d_k, d_v
+    multiples of 8 (zero-padded to 128-wide tiles); the rest is fp32 CUDA-core."""
+    return dtype == "bf16" and C == 64 and dk % 8 == 0 and dk <= 128 and dv % 8 == 0
+
+
 @pytest.mark.parametrize("dk,dv", [(16, 16), (64, 64), (128, 128), (64, 128), (128, 64),
-                                   (128, 256), (96, 192), (40, 24)])
+                                   (128, 256), (96, 192), (40, 24), (8, 8), (128, 200),
+                                   (72, 136), (100, 36), (20, 20)])
 def test_head_dims(gdn, dk, dv):
     x = I.custom(1, 2, 300, dk, dv, 64, dtype="bf16", seed=dk * 1000 + dv, s0="normal_0.02")
     run_and_check(gdn, x, 64, "bf16")
+    assert gdn.gdn_last_launch_count()[1] == (1 if tc_path_expected(dk, dv, 64, "bf16") else 0)
+
+
+def test_hybrid_head_shape_extended_beta_varlen(gdn):
+    """d_k = 96, d_v = 192 (two d_v tiles, the second half padding), beta in
+    (0, 2), packed ragged sequences with an initial state: tensor-core path."""
+    lens = [1, 64, 100, 255, 0, 129]
+    x = I.custom(1, 6, 0, 96, 192, 64, dtype="bf16", seed=21, lengths=lens,
+                 s0="normal_0.02", beta="uniform_0_2")
+    assert float(x["beta"].max()) > 1.5
+    run_and_check(gdn, x, 64, "bf16")
+    assert gdn.gdn_last_launch_count() == (1, 1)
 
 
 def test_varlen_edge_lengths(gdn):
