@@ -48,6 +48,22 @@ def gdn_chunk_fwd(q, k, v, log_alpha, beta, S0=None, o=None, S_final=None,
     allocated here.  Runs on ``stream`` (a torch.cuda.Stream, a raw handle, or
     None for the current torch stream).
     """
+    return _chunk(q, k, v, log_alpha, beta, None, S0, o, S_final, C, cu_seqlens, stream,
+                  want_final_state)
+
+
+def gdn_chunk_fwd_eta(q, k, v, log_alpha, beta, eta, S0=None, o=None, S_final=None,
+                      C=64, cu_seqlens=None, stream=None, want_final_state=True):
+    """``gdn_chunk_fwd`` with a write strength ``eta`` [B,T,H] fp32 separate
+    from the erase strength ``beta``: S_t = alpha S (I - beta k k^T) + eta v k^T."""
+    if eta is None:
+        raise ValueError("eta is required (use gdn_chunk_fwd for eta = beta)")
+    return _chunk(q, k, v, log_alpha, beta, eta, S0, o, S_final, C, cu_seqlens, stream,
+                  want_final_state)
+
+
+def _chunk(q, k, v, log_alpha, beta, eta, S0, o, S_final, C, cu_seqlens, stream,
+           want_final_state):
     lib = _lib.load()
     if q.dtype not in _DTYPES:
         raise TypeError("q/k/v dtype must be float32 or bfloat16, got %s" % q.dtype)
@@ -55,6 +71,7 @@ def gdn_chunk_fwd(q, k, v, log_alpha, beta, S0=None, o=None, S_final=None,
         _need_cuda(name, t, q.dtype)
     _need_cuda("log_alpha", log_alpha, torch.float32)
     _need_cuda("beta", beta, torch.float32)
+    _need_cuda("eta", eta, torch.float32)
     _need_cuda("S0", S0, torch.float32)
     _need_cuda("cu_seqlens", cu_seqlens, torch.int32)
     if q.dim() != 4 or k.shape != q.shape or v.dim() != 4 or v.shape[:3] != q.shape[:3]:
@@ -63,6 +80,8 @@ def gdn_chunk_fwd(q, k, v, log_alpha, beta, S0=None, o=None, S_final=None,
     dv = v.shape[-1]
     if log_alpha.shape != (B, T, H) or beta.shape != (B, T, H):
         raise ValueError("log_alpha and beta must be [B,T,H]")
+    if eta is not None and eta.shape != (B, T, H):
+        raise ValueError("eta must be [B,T,H]")
     if cu_seqlens is not None:
         if B != 1:
             raise ValueError("packed (cu_seqlens) inputs must have B == 1")
@@ -77,17 +96,18 @@ def gdn_chunk_fwd(q, k, v, log_alpha, beta, S0=None, o=None, S_final=None,
     if S_final is None and want_final_state:
         S_final = torch.empty((N, H, dv, dk), dtype=torch.float32, device=q.device)
     _need_cuda("S_final", S_final, torch.float32)
-    if stream is None:
-        handle = torch.cuda.current_stream(q.device).cuda_stream
-    elif isinstance(stream, torch.cuda.Stream):
-        handle = stream.cuda_stream
-    else:
-        handle = int(stream)
+    handle = ctypes.c_void_p(_stream_handle(stream, q.device))
     with torch.cuda.device(q.device):
-        st = lib.gdn_chunk_fwd(
-            _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(S0),
-            _ptr(o), _ptr(S_final), N, H, T, dk, dv, int(C), _ptr(cu_seqlens),
-            _DTYPES[q.dtype], ctypes.c_void_p(handle))
+        if eta is None:
+            st = lib.gdn_chunk_fwd(
+                _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(S0),
+                _ptr(o), _ptr(S_final), N, H, T, dk, dv, int(C), _ptr(cu_seqlens),
+                _DTYPES[q.dtype], handle)
+        else:
+            st = lib.gdn_chunk_fwd_eta(
+                _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(eta), _ptr(S0),
+                _ptr(o), _ptr(S_final), N, H, T, dk, dv, int(C), _ptr(cu_seqlens),
+                _DTYPES[q.dtype], handle)
     _lib.check(st)
     return o, S_final
 

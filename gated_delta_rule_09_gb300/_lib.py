@@ -28,6 +28,8 @@ _i = ctypes.c_int
 SIGNATURES = {
     "gdn_chunk_fwd": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                                      _i, _i, _i, _i, _i, _i, _vp, _i, _vp]),
+    "gdn_chunk_fwd_eta": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                                         _i, _i, _i, _i, _i, _i, _vp, _i, _vp]),
     "gdn_decode_step": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                                        _i, _i, _i, _i, _i, _i, _vp]),
     "gdn_get_device_status": (ctypes.c_int, [_vp, ctypes.POINTER(ctypes.c_uint)]),

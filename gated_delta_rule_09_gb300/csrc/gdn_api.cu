@@ -55,6 +55,85 @@ bool overlaps(const void *a, size_t na, const void *b, size_t nb)
 
 bool aligned(const void *p, size_t al) { return (reinterpret_cast<uintptr_t>(p) % al) == 0; }
 
+gdn_status_t chunk_fwd(const void *q, const void *k, const void *v, const float *log_alpha,
+                       const float *beta, const float *eta, const float *S0, void *o,
+                       float *S_final, int B, int H, int T, int d_k, int d_v, int C,
+                       const int32_t *cu_seqlens, gdn_dtype_t dtype, void *stream)
+{
+    t_msg[0] = '\0';
+    if (B < 0 || H < 0 || T < 0)
+        return fail(GDN_ERR_INVALID_ARG, "negative size: B=%d H=%d T=%d", B, H, T);
+    if (d_k < 1 || d_v < 1)
+        return fail(GDN_ERR_INVALID_ARG, "head dims must be >= 1: d_k=%d d_v=%d", d_k, d_v);
+    if (dtype != GDN_F32 && dtype != GDN_BF16)
+        return fail(GDN_ERR_UNSUPPORTED, "dtype %d (expected GDN_F32 or GDN_BF16)", (int)dtype);
+    if (C != 16 && C != 32 && C != 64)
+        return fail(GDN_ERR_UNSUPPORTED, "chunk length C=%d (supported: 16, 32, 64)", C);
+    if (d_k > 128)
+        return fail(GDN_ERR_UNSUPPORTED, "d_k=%d (supported: 1..128)", d_k);
+    if (cu_seqlens && B < 1)
+        return fail(GDN_ERR_INVALID_ARG, "cu_seqlens given with B=%d sequences", B);
+
+    const size_t esz = dtype == GDN_BF16 ? 2 : 4;
+    const size_t tokens = cu_seqlens ? (size_t)T : (size_t)B * T;  // token rows
+    const size_t nqk = tokens * H * d_k * esz, nv = tokens * H * d_v * esz;
+    const size_t ng = tokens * H * sizeof(float);
+    const size_t ns = (size_t)B * H * d_v * d_k * sizeof(float);
+    const bool work = tokens > 0 && H > 0;
+    const bool any_units = (size_t)B * H > 0;
+
+    if (work && (!q || !k || !v || !log_alpha || !beta || !o))
+        return fail(GDN_ERR_INVALID_ARG, "q, k, v, log_alpha, beta and o must be non-NULL");
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16))
+        return fail(GDN_ERR_INVALID_ARG, "q, k, v and o must be 16-byte aligned");
+    if (!aligned(log_alpha, 4) || !aligned(beta, 4) || !aligned(eta, 4) || !aligned(S0, 4) ||
+        !aligned(S_final, 4))
+        return fail(GDN_ERR_INVALID_ARG,
+                    "log_alpha, beta, eta, S0 and S_final must be 4-byte aligned");
+    if (overlaps(o, nv, q, nqk) || overlaps(o, nv, k, nqk) || overlaps(o, nv, v, nv) ||
+        overlaps(o, nv, log_alpha, ng) || overlaps(o, nv, beta, ng) || overlaps(o, nv, eta, ng) ||
+        overlaps(o, nv, S0, ns) || overlaps(o, nv, S_final, ns))
+        return fail(GDN_ERR_INVALID_ARG, "o overlaps another argument");
+    if (S_final && S_final != S0 &&
+        (overlaps(S_final, ns, q, nqk) || overlaps(S_final, ns, k, nqk) ||
+         overlaps(S_final, ns, v, nv) || overlaps(S_final, ns, log_alpha, ng) ||
+         overlaps(S_final, ns, beta, ng) || overlaps(S_final, ns, eta, ng) ||
+         overlaps(S_final, ns, S0, ns)))
+        return fail(GDN_ERR_INVALID_ARG, "S_final overlaps an input (only S_final == S0 is allowed)");
+
+    t_launches = 0;
+    t_path = -1;
+    if (!any_units) return GDN_OK;
+    if (!work && !S_final) return GDN_OK;  // nothing to compute, nothing to write
+
+    GdnArgs a;
+    a.q = q; a.k = k; a.v = v; a.log_alpha = log_alpha; a.beta = beta; a.eta = eta; a.S0 = S0;
+    a.o = o; a.S_final = S_final;
+    a.N = B; a.H = H; a.T = T; a.dk = d_k; a.dv = d_v; a.C = C;
+    a.cu_seqlens = cu_seqlens;
+    a.dtype = dtype == GDN_BF16 ? 1 : 0;
+    gdn_status_t st = status_word(&a.status);
+    if (st != GDN_OK) return st;
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int launches = 0;
+    cudaError_t e;
+    int path;
+    if (gdn_tc_supported(a)) {
+        e = gdn_launch_tc(a, s, &launches);
+        path = 1;
+    } else {
+        e = gdn_launch_simt(a, s, &launches);
+        path = 0;
+    }
+    if (e != cudaSuccess)
+        return fail(GDN_ERR_CUDA, "kernel launch (%s path): %s",
+                    path ? "tcgen05" : "fp32", cudaGetErrorString(e));
+    t_launches = launches;
+    t_path = path;
+    return GDN_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -94,75 +173,23 @@ gdn_status_t gdn_chunk_fwd(const void *q, const void *k, const void *v,
                            const int32_t *cu_seqlens, gdn_dtype_t dtype,
                            void *stream)
 {
-    t_msg[0] = '\0';
-    if (B < 0 || H < 0 || T < 0)
-        return fail(GDN_ERR_INVALID_ARG, "negative size: B=%d H=%d T=%d", B, H, T);
-    if (d_k < 1 || d_v < 1)
-        return fail(GDN_ERR_INVALID_ARG, "head dims must be >= 1: d_k=%d d_v=%d", d_k, d_v);
-    if (dtype != GDN_F32 && dtype != GDN_BF16)
-        return fail(GDN_ERR_UNSUPPORTED, "dtype %d (expected GDN_F32 or GDN_BF16)", (int)dtype);
-    if (C != 16 && C != 32 && C != 64)
-        return fail(GDN_ERR_UNSUPPORTED, "chunk length C=%d (supported: 16, 32, 64)", C);
-    if (d_k > 128)
-        return fail(GDN_ERR_UNSUPPORTED, "d_k=%d (supported: 1..128)", d_k);
-    if (cu_seqlens && B < 1)
-        return fail(GDN_ERR_INVALID_ARG, "cu_seqlens given with B=%d sequences", B);
+    return chunk_fwd(q, k, v, log_alpha, beta, nullptr, S0, o, S_final, B, H, T, d_k, d_v, C,
+                     cu_seqlens, dtype, stream);
+}
 
-    const size_t esz = dtype == GDN_BF16 ? 2 : 4;
-    const size_t tokens = cu_seqlens ? (size_t)T : (size_t)B * T;  // token rows
-    const size_t nqk = tokens * H * d_k * esz, nv = tokens * H * d_v * esz;
-    const size_t ng = tokens * H * sizeof(float);
-    const size_t ns = (size_t)B * H * d_v * d_k * sizeof(float);
-    const bool work = tokens > 0 && H > 0;
-    const bool any_units = (size_t)B * H > 0;
-
-    if (work && (!q || !k || !v || !log_alpha || !beta || !o))
-        return fail(GDN_ERR_INVALID_ARG, "q, k, v, log_alpha, beta and o must be non-NULL");
-    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16))
-        return fail(GDN_ERR_INVALID_ARG, "q, k, v and o must be 16-byte aligned");
-    if (!aligned(log_alpha, 4) || !aligned(beta, 4) || !aligned(S0, 4) || !aligned(S_final, 4))
-        return fail(GDN_ERR_INVALID_ARG, "log_alpha, beta, S0 and S_final must be 4-byte aligned");
-    if (overlaps(o, nv, q, nqk) || overlaps(o, nv, k, nqk) || overlaps(o, nv, v, nv) ||
-        overlaps(o, nv, log_alpha, ng) || overlaps(o, nv, beta, ng) || overlaps(o, nv, S0, ns) ||
-        overlaps(o, nv, S_final, ns))
-        return fail(GDN_ERR_INVALID_ARG, "o overlaps another argument");
-    if (S_final && S_final != S0 &&
-        (overlaps(S_final, ns, q, nqk) || overlaps(S_final, ns, k, nqk) ||
-         overlaps(S_final, ns, v, nv) || overlaps(S_final, ns, log_alpha, ng) ||
-         overlaps(S_final, ns, beta, ng) || overlaps(S_final, ns, S0, ns)))
-        return fail(GDN_ERR_INVALID_ARG, "S_final overlaps an input (only S_final == S0 is allowed)");
-
-    t_launches = 0;
-    t_path = -1;
-    if (!any_units) return GDN_OK;
-    if (!work && !S_final) return GDN_OK;  // nothing to compute, nothing to write
-
-    GdnArgs a;
-    a.q = q; a.k = k; a.v = v; a.log_alpha = log_alpha; a.beta = beta; a.S0 = S0;
-    a.o = o; a.S_final = S_final;
-    a.N = B; a.H = H; a.T = T; a.dk = d_k; a.dv = d_v; a.C = C;
-    a.cu_seqlens = cu_seqlens;
-    a.dtype = dtype == GDN_BF16 ? 1 : 0;
-    gdn_status_t st = status_word(&a.status);
-    if (st != GDN_OK) return st;
-
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    int launches = 0;
-    cudaError_t e;
-    int path;
-    if (gdn_tc_supported(a)) {
-        e = gdn_launch_tc(a, s, &launches);
-        path = 1;
-    } else {
-        e = gdn_launch_simt(a, s, &launches);
-        path = 0;
+gdn_status_t gdn_chunk_fwd_eta(const void *q, const void *k, const void *v,
+                               const float *log_alpha, const float *beta, const float *eta,
+                               const float *S0, void *o, float *S_final,
+                               int B, int H, int T, int d_k, int d_v, int C,
+                               const int32_t *cu_seqlens, gdn_dtype_t dtype,
+                               void *stream)
+{
+    if (!eta && B > 0 && H > 0 && T > 0) {
+        t_msg[0] = '\0';
+        return fail(GDN_ERR_INVALID_ARG, "eta must be non-NULL (use gdn_chunk_fwd for eta = beta)");
     }
-    if (e != cudaSuccess)
-        return fail(GDN_ERR_CUDA, "kernel launch (%s path): %s",
-                    path ? "tcgen05" : "fp32", cudaGetErrorString(e));
-    t_launches = launches;
-    t_path = path;
-    return GDN_OK;
+    return chunk_fwd(q, k, v, log_alpha, beta, eta, S0, o, S_final, B, H, T, d_k, d_v, C,
+                     cu_seqlens, dtype, stream);
 }
 
 gdn_status_t gdn_decode_step(const void *q, const void *k, const void *v,

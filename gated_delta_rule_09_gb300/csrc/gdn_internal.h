@@ -8,6 +8,7 @@ struct GdnArgs {
     const void *q, *k, *v;       // [*, T, H, dk] / [*, T, H, dv], dtype
     const float *log_alpha;      // [*, T, H]
     const float *beta;           // [*, T, H]
+    const float *eta;            // [*, T, H] write strength, or null (= beta)
     const float *S0;             // [N, H, dv, dk] or null
     void *o;                     // [*, T, H, dv], dtype
     float *S_final;              // [N, H, dv, dk] or null

@@ -9,7 +9,8 @@
 //   A      StrictLower(diag(beta) K K^T * e^{g_i - g_j})        (§"UT transform")
 //   T      (I + A)^{-1} by column-wise forward substitution
 //          ("RNN的复兴03：现代RNN的并行计算", §2.3.1, with the sign of A flipped)
-//   W, U   T diag(beta) (K * e^g),  T diag(beta) V               (§"S 的推导")
+//   W, U   T diag(beta) (K * e^g),  T diag(eta) V                (§"S 的推导";
+//          eta, the write strength, is beta unless given)
 //   V_new  U - W S^T
 //   O      (Q * e^g) S^T + (Q K^T * e^{g_i - g_j}, j <= i) V_new (§"O 的推导")
 //   S      e^{g_last} S + V_new^T (K * e^{g_last - g})          (§"S 的推导")
@@ -79,6 +80,7 @@ gdn_simt_kernel(GdnArgs a)
     float *eg = g + C;              // [C]  e^{g_i}
     float *ek = eg + C;             // [C]  e^{g_last - g_i}
     float *bt = ek + C;             // [C]  beta
+    float *et = bt + C;             // [C]  eta (the write strength; beta unless given)
 
     const size_t sbase = ((size_t)n * H + h) * dv * dk;
     for (int idx = tid; idx < kDvt * dk; idx += kThreads) {
@@ -109,14 +111,16 @@ gdn_simt_kernel(GdnArgs a)
             Vs[i * ldv + r] = x;
         }
         if (tid < C) {
-            float la = 0.f, b = 0.f;
+            float la = 0.f, b = 0.f, e = 0.f;
             if (tid < nc) {
                 const size_t gi = (size_t)(start + c0 + tid) * H + h;
                 la = a.log_alpha[gi];
                 b = a.beta[gi];
+                e = a.eta ? a.eta[gi] : b;
             }
             g[tid] = la;
             bt[tid] = b;
+            et[tid] = e;
         }
         __syncthreads();
         if (tid == 0) {  // inclusive cumulative sum (padding rows add 0)
@@ -159,7 +163,7 @@ gdn_simt_kernel(GdnArgs a)
             }
         }
         __syncthreads();
-        // W = T diag(beta) (K * e^g),  U = T diag(beta) V
+        // W = T diag(beta) (K * e^g),  U = T diag(eta) V
         for (int idx = tid; idx < C * dk; idx += kThreads) {
             const int i = idx / dk, c = idx % dk;
             float acc = 0.f;
@@ -171,7 +175,7 @@ gdn_simt_kernel(GdnArgs a)
             const int i = idx / kDvt, r = idx % kDvt;
             float acc = 0.f;
             for (int j = 0; j <= i; ++j)
-                acc = fmaf(Ts[i * ldc + j], bt[j] * Vs[j * ldv + r], acc);
+                acc = fmaf(Ts[i * ldc + j], et[j] * Vs[j * ldv + r], acc);
             Us[i * ldv + r] = acc;
         }
         __syncthreads();
@@ -221,7 +225,7 @@ gdn_simt_kernel(GdnArgs a)
 size_t gdn_simt_smem_bytes(int C, int dk)
 {
     const size_t ldk = dk + 1, ldc = C + 1, ldv = kDvt + 1;
-    return sizeof(float) * (3 * C * ldk + kDvt * ldk + 3 * C * ldc + 2 * C * ldv + 4 * C);
+    return sizeof(float) * (3 * C * ldk + kDvt * ldk + 3 * C * ldc + 2 * C * ldv + 5 * C);
 }
 
 cudaError_t gdn_launch_simt(const GdnArgs &a, cudaStream_t s, int *launches)

@@ -11,7 +11,8 @@
 //   state-independent:  A = StrictLower(diag(beta) K K^T * e^{g_i-g_j})
 //                       P = Lower(Q K^T * e^{g_i-g_j})
 //                       T = (I + A)^{-1}
-//                       T'' = T diag(beta e^g),   T' = T diag(beta)
+//                       T'' = T diag(beta e^g),   T' = T diag(eta)
+//                       (eta, the write strength, is beta unless given)
 //                       W^T = K^T T''^T,          U^T = V^T T'^T
 //   state chain:        V_new^T = U^T - S W^T
 //                       O^T = e^{g} (S Q^T) + V_new^T P^T
@@ -68,7 +69,7 @@ constexpr int kLdX3 = 36;    // row stride of the 32x32 merge scratch
 
 // ---- a ring slot: what the producer ships, then the consumer's own tiles
 constexpr int kOutP = 0;           // P rows i (K-major), fp16
-constexpr int kOutTp = 8192;       // T' = T diag(beta) rows j (K-major), fp16
+constexpr int kOutTp = 8192;       // T' = T diag(eta) rows j (K-major), fp16
 constexpr int kOutTpp = 16384;     // T'' = T diag(beta e^g) rows j (K-major), fp16
 constexpr int kOutG = 24576;       // g[64], e^g[64], e^{g_C-g}[64] fp32
 constexpr int kOutBytes = 25600;   // shipped per chunk (distributed shared memory moves
@@ -95,7 +96,7 @@ constexpr int kSmemBytes =
     (kCOffSmall > kPOffSmall ? kCOffSmall : kPOffSmall) + kSmallBytes + 1024;
 
 struct PSmall {
-    float scan[2][kC], beta[2][kC], colf[2][kC], colb[2][kC];
+    float scan[2][kC], beta[2][kC], eta[2][kC], colf[2][kC], colb[2][kC];
     uint64_t tma_in[2], mma[2], slot_empty[2];
     uint32_t tmem;
     int abort_flag;
@@ -268,16 +269,18 @@ __device__ __forceinline__ void producer(const GdnArgs &a, const CUtensorMap *tm
             tma_load_3d(in + b * 16384 + 8192, tm_q, &s->tma_in[p], b * 64, h, z);
         }
     };
-    float la_next = 0.f, b_next = 0.f;
+    float la_next = 0.f, b_next = 0.f, e_next = 0.f;
     auto load_gates = [&](int c) {
         la_next = 0.f;
         b_next = 0.f;
+        e_next = 0.f;
         if (t < kC && c < nchunks) {
             const long tt = (long)c * kC + t;
             if (tt < len) {
                 const size_t gi = (size_t)(start + tt) * a.H + h;
                 la_next = a.log_alpha[gi];
                 b_next = a.beta[gi];
+                e_next = a.eta ? a.eta[gi] : b_next;
             }
         }
     };
@@ -294,7 +297,7 @@ __device__ __forceinline__ void producer(const GdnArgs &a, const CUtensorMap *tm
         float *gout = reinterpret_cast<float *>(out + kOutG);
 
         // decay: g = inclusive cumulative sum of log alpha (padding adds 0)
-        const float la = la_next, bt = b_next;
+        const float la = la_next, bt = b_next, et = e_next;
         load_gates(c + 2);
         if (t < kC) {
             float x = la;
@@ -305,6 +308,7 @@ __device__ __forceinline__ void producer(const GdnArgs &a, const CUtensorMap *tm
             }
             s->scan[p][t] = x;
             s->beta[p][t] = bt;
+            s->eta[p][t] = et;
         }
         named_sync(bar_id, 128);
         if (t < kC) gout[t] = s->scan[p][t] + (t >= 32 ? s->scan[p][31] : 0.f);
@@ -506,12 +510,12 @@ __device__ __forceinline__ void producer(const GdnArgs &a, const CUtensorMap *tm
                 make_float4(-a1c.x, -a1c.y, -a1c.z, -a1c.w);
         }
         named_sync(bar_id, 128);
-        // T'' = T diag(beta e^g) and T' = T diag(beta), both shipped
+        // T'' = T diag(beta e^g) and T' = T diag(eta), both shipped
         {
             const bool first = t < kC;
             const int j = first ? t : t - kC;
             uint8_t *dst = first ? out + kOutTpp : out + kOutTp;
-            const float *scale = first ? s->colb[p] : s->beta[p];
+            const float *scale = first ? s->colb[p] : s->eta[p];
             float x[8];
 #pragma unroll 1
             for (int q = 0; q < 8; ++q) {

@@ -3,7 +3,7 @@
 This module is shared by the tests, the benchmark and the smoke check; it
 holds no step of the method itself, only the input distributions.  Every
 tensor is drawn in fp64 from ``numpy.random.default_rng(seed)`` in a fixed
-order (sequence lengths, q, k, v, beta, alpha or log alpha, S0), normalised
+order (sequence lengths, q, k, v, beta, alpha or log alpha, S0, eta), normalised
 in fp64 where a workload asks for unit-norm keys or queries, then rounded once
 to the workload's dtype (round-to-nearest-even for bf16).  The oracle sees the
 same rounded values widened back to fp64.
@@ -60,6 +60,7 @@ class Workload:
     varlen: bool = False
     len_lo: int = 0
     len_hi: int = 0
+    eta_dist: str = "none"  # "none" | "uniform": a write strength separate from beta
 
 
 WORKLOADS = {
@@ -140,6 +141,7 @@ def generate(w: Workload, seed: int = 0, lengths=None, S0: Optional[str] = None)
         S0t = rng.normal(0.0, 0.02, (N, H, dv, dk))
     else:
         S0t = None
+    eta = rng.uniform(0.0, 1.0, (Bt, Tt, H)) if w.eta_dist == "uniform" else None
     dt = TORCH_DTYPE[w.dtype]
     out = dict(
         q=torch.from_numpy(q).to(dt),
@@ -149,16 +151,18 @@ def generate(w: Workload, seed: int = 0, lengths=None, S0: Optional[str] = None)
         beta=torch.from_numpy(beta).to(torch.float32),
         S0=None if S0t is None else torch.from_numpy(S0t).to(torch.float32),
         cu_seqlens=None if cu is None else torch.from_numpy(cu),
+        eta=None if eta is None else torch.from_numpy(eta).to(torch.float32),
         N=N, lengths=lengths,
     )
     return out
 
 
 def custom(B, H, T, dk, dv, C, dtype="bf16", seed=0, lengths=None,
-           s0="none", alpha="softplus_0.1", beta="sigmoid_normal", q_unit=True):
-    """Inputs of arbitrary shape with the small_bf16 distributions by default."""
+           s0="none", alpha="softplus_0.1", beta="sigmoid_normal", q_unit=True, eta="none"):
+    """Inputs of arbitrary shape with the small_bf16 distributions by default
+    (``eta="uniform"`` adds a write strength eta ~ U(0,1), drawn last)."""
     w = Workload("custom", B if lengths is None else len(lengths), H, T, dk, dv,
-                 C, dtype, q_unit, beta, alpha, s0, varlen=lengths is not None)
+                 C, dtype, q_unit, beta, alpha, s0, varlen=lengths is not None, eta_dist=eta)
     return generate(w, seed=seed, lengths=lengths)
 
 

@@ -112,6 +112,25 @@ gdn_status_t gdn_chunk_fwd(const void *q, const void *k, const void *v,
                            void *stream);
 
 /*
+ * gdn_chunk_fwd_eta — gdn_chunk_fwd with a write strength eta_t separate
+ * from the erase strength beta_t ("RNN的复兴03：现代RNN的并行计算", §一, the
+ * general delta-rule recurrence):
+ *
+ *     S_t = alpha_t S_{t-1} (I - beta_t k_t k_t^T) + eta_t v_t k_t^T
+ *
+ * In the chunk form only U changes, U = T diag(eta) V; A and W keep beta.
+ * With eta = beta this is gdn_chunk_fwd.  eta is fp32 [B, T, H] (the layout
+ * of beta), non-NULL when there is work, 4-byte aligned and not overlapping
+ * o or S_final.  Every other argument, and every rule, is gdn_chunk_fwd's.
+ */
+gdn_status_t gdn_chunk_fwd_eta(const void *q, const void *k, const void *v,
+                               const float *log_alpha, const float *beta, const float *eta,
+                               const float *S0, void *o, float *S_final,
+                               int B, int H, int T, int d_k, int d_v, int C,
+                               const int32_t *cu_seqlens, gdn_dtype_t dtype,
+                               void *stream);
+
+/*
  * gdn_decode_step — the same recurrence evaluated token by token, for decoding
  * ("从零开始的 GDN 推导", recurrent form of the gated delta rule;
  * "RNN的复兴03：现代RNN的并行计算", §一, delta-rule update), batched over

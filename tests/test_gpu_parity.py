@@ -177,3 +177,48 @@ def test_sampled_outputs_at_full_size_train_shape(gdn):
                                     x["log_alpha"][sl], x["beta"][sl])
         assert err(o[sl], ro, "bf16") <= TOL_BF16
         assert err(S[b:b + 1, h:h + 1], rS, "bf16", rounded=False) <= TOL_BF16
+
+
+@pytest.mark.parametrize("dtype,dk,dv,C", [("bf16", 128, 128, 64), ("f32", 32, 48, 16),
+                                           ("bf16", 96, 192, 64), ("bf16", 40, 36, 32)])
+def test_write_strength_eta(gdn, dtype, dk, dv, C):
+    """S_t = alpha S (I - beta k k^T) + eta v k^T with eta independent of beta,
+    on both kernels, against the oracle's eta form."""
+    x = I.custom(2, 3, 200, dk, dv, C, dtype=dtype, seed=31 + dk + C, s0="normal_0.02",
+                 eta="uniform")
+    d = _dev(x)
+    o, S = gdn.gdn_chunk_fwd_eta(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], d["eta"],
+                                 S0=d["S0"], C=C)
+    assert gdn.gdn_get_device_status() == 0
+    assert gdn.gdn_last_launch_count()[1] == (1 if tc_path_expected(dk, dv, C, dtype) else 0)
+    ro, rS = gdn_recurrence_f64(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"],
+                                S0=x["S0"], eta=x["eta"])
+    tol = TOL_F32 if dtype == "f32" else TOL_BF16
+    assert err(o.double().cpu().numpy(), ro, dtype) <= tol
+    assert err(S.double().cpu().numpy(), rS, dtype, rounded=False) <= tol
+
+
+@pytest.mark.parametrize("dtype,C", [("bf16", 64), ("f32", 32)])
+def test_eta_equal_beta_is_gdn_chunk_fwd(gdn, dtype, C):
+    x = I.custom(1, 4, 150, 64, 64, C, dtype=dtype, seed=33, s0="normal_0.02")
+    d = _dev(x)
+    a = gdn.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], S0=d["S0"], C=C)
+    b = gdn.gdn_chunk_fwd_eta(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"],
+                              d["beta"].clone(), S0=d["S0"], C=C)
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+def test_eta_linear_attention_limit(gdn):
+    """alpha = 1, beta = 0, eta = 1: nothing is erased, every value is
+    written, and the output is causal linear attention on top of S0 (the
+    oracle is pinned to that closed form on the CPU)."""
+    x = I.custom(2, 2, 130, 128, 128, 64, dtype="bf16", seed=34, s0="normal_0.02", alpha="one")
+    x["beta"] = torch.zeros_like(x["beta"])
+    eta = torch.ones_like(x["beta"])
+    d = _dev(x)
+    o, S = gdn.gdn_chunk_fwd_eta(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], eta.cuda(),
+                                 S0=d["S0"], C=64)
+    ro, rS = gdn_recurrence_f64(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"],
+                                S0=x["S0"], eta=eta)
+    assert err(o.double().cpu().numpy(), ro, "bf16") <= TOL_BF16
+    assert err(S.double().cpu().numpy(), rS, "bf16", rounded=False) <= TOL_BF16

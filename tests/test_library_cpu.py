@@ -115,3 +115,13 @@ def test_decode_host_validation(lib, kw, code):
 def test_decode_empty_problem_is_a_no_op(lib):
     assert _dcall(lib, N=0) == 0
     assert _dcall(lib, H=0, So=None) == 0
+
+
+def test_eta_entry_point_validation(lib):
+    # eta is required when there is work; misaligned or overlapping eta is rejected
+    f = lambda eta, o=0x500000: lib.gdn_chunk_fwd_eta(0x1000, 0x100000, 0x200000, 0x300000,
+                                                       0x400000, eta, None, o, None, 1, 1, 16,
+                                                       16, 16, 16, None, 1, None)
+    assert f(None) == 1 and lib.gdn_get_last_error()
+    assert f(0x700002) == 1
+    assert f(0x500010) == 1      # eta inside o
