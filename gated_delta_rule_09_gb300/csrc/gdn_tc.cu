@@ -21,11 +21,13 @@
 // Each unit runs on a cluster of two CTAs on two SMs:
 //
 //  * rank 0, the producer, computes A, P, T, T' and T'' for every chunk with
-//    two 4-warp pipelines (even and odd chunks): TMA loads of the q/k tiles,
-//    [K;Q] K^T on the tensor cores, A and P on the CUDA cores, the blocked
-//    inverse, and ships P, T', T'' and the decay vectors (25 KB) into the
-//    consumer's ring slot with one distributed-shared-memory bulk copy that
-//    completes on the consumer's mbarrier.
+//    three 4-warp pipelines (chunk c on pipeline c % 3; each pipeline's work
+//    is one long dependent chain, so more pipelines means more chunks in
+//    flight): TMA loads of the q/k tiles, [K;Q] K^T on the tensor cores, A
+//    and P on the CUDA cores, the blocked inverse, and ships P, T', T'' and
+//    the decay vectors (25 KB) into the consumer's ring slot, in chunk order,
+//    with distributed-shared-memory bulk copies that complete on the
+//    consumer's mbarrier.
 //  * rank 1, the consumer, keeps the state slice (128 x 128 fp32) in TMEM for
 //    the whole walk and loads its own q/k/v tiles by TMA.  Warps 0-3 run the
 //    state chain (fp16 copy of S, S W^T and S Q^T, V_new, V_new^T P^T and the
@@ -60,7 +62,9 @@ using namespace sm100;
 constexpr int kC = 64;       // chunk length
 constexpr int kDK = 128;     // d_k as the tiles hold it (a smaller d_k is zero-padded)
 constexpr int kDVT = 128;    // d_v rows per unit (rows past d_v are zero padding)
-constexpr int kThreads = 384;  // producer: 2 x 4 warps (warps 8-11 idle); consumer: 3 x 4 warps
+constexpr int kThreads = 384;  // producer: 3 pipelines x 4 warps; consumer: 3 x 4 warps
+constexpr int kNP = 3;         // producer pipelines (chunk c goes to pipeline c % 3)
+constexpr int kNOut = 5;       // outgoing buffers (chunk c uses buffer c % 5)
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
 constexpr float kF16Max = 65504.f;
 constexpr int kLdA = 68;     // fp32 row stride of A / T: 16-byte rows, 4-bank offset per row
@@ -72,32 +76,38 @@ constexpr int kOutP = 0;           // P rows i (K-major), fp16
 constexpr int kOutTp = 8192;       // T' = T diag(eta) rows j (K-major), fp16
 constexpr int kOutTpp = 16384;     // T'' = T diag(beta e^g) rows j (K-major), fp16
 constexpr int kOutG = 24576;       // g[64], e^g[64], e^{g_C-g}[64] fp32
-constexpr int kOutBytes = 25600;   // shipped per chunk (distributed shared memory moves
-                                   // ~20 bytes per cycle, so only what the consumer
-                                   // cannot load itself is shipped)
+constexpr int kGBytes = 3 * 64 * 4;
+constexpr int kOutBytes = 25600;   // slot room for the shipped part (distributed shared
+                                   // memory moves ~20 bytes per cycle, so only what the
+                                   // consumer cannot load itself is shipped)
 constexpr int kSlotKQ = kOutBytes;         // [K rows | Q rows] per d_k half, fp16 after conversion
 constexpr int kSlotV = kSlotKQ + 32768;    // V, 2 d_v halves (later V_new * e^{g_C-g})
 constexpr int kSlotBytes = kSlotV + 16384;
 
-// ---- producer shared memory (per pipeline p = 0, 1)
-constexpr int kPIn = 32768;                        // [K | Q] per d_k half, bf16 (TMA)
-constexpr int kPAT = 22528;                        // fp32 A then T in place [64][68] | X[32][36]
+// ---- producer shared memory
+// Per pipeline one 32 KB buffer: the [K | Q] tiles (bf16, TMA) until the
+// [K;Q] K^T MMA has read them, then A and T in place (fp32 [64][68]) and the
+// merge scratch; the next TMA into it follows the T build.
+constexpr int kPIn = 32768;
+constexpr int kPXs = kC * kLdA * 4;                // merge scratch offset inside the buffer
 constexpr int kPOffIn = 0;
-constexpr int kPOffOut = kPOffIn + 2 * kPIn;        // 2 pipelines x 2 outgoing buffers
-constexpr int kPOffAT = kPOffOut + 4 * kOutBytes;
-constexpr int kPOffSmall = kPOffAT + 2 * kPAT;
+constexpr int kPOffOut = kPOffIn + kNP * kPIn;      // outgoing P | T' | T'' pool (kNOut x 24 KB)
+constexpr int kPOffSmall = kPOffOut + kNOut * kOutG;
 // ---- consumer shared memory
 constexpr int kCOffW = 2 * kSlotBytes;             // W^T rows d (MN-major B operand), fp16
 constexpr int kCOffSb = kCOffW + 16384;            // S as fp16, 2 d_k halves x 128 rows
 constexpr int kCOffVnT = kCOffSb + 32768;          // V_new^T rows v (K-major), fp16
 constexpr int kCOffSmall = kCOffVnT + 16384;
-constexpr int kSmallBytes = 3072;
-constexpr int kSmemBytes =
-    (kCOffSmall > kPOffSmall ? kCOffSmall : kPOffSmall) + kSmallBytes + 1024;
+constexpr int kCSmallBytes = 3072;
+constexpr int kPSmallBytes = 8192;
+constexpr int kSmemBytes = (kCOffSmall + kCSmallBytes > kPOffSmall + kPSmallBytes
+                                ? kCOffSmall + kCSmallBytes
+                                : kPOffSmall + kPSmallBytes) + 1024;
 
 struct PSmall {
-    float scan[2][kC], beta[2][kC], eta[2][kC], colf[2][kC], colb[2][kC];
-    uint64_t tma_in[2], mma[2], slot_empty[2];
+    float g[kNOut][3 * kC];   // outgoing g, e^g, e^{g_C-g} (second bulk copy), pool as the tiles
+    float scan[kNP][kC], beta[kNP][kC], eta[kNP][kC], colf[kNP][kC], colb[kNP][kC];
+    uint64_t tma_in[kNP], mma[kNP], shipped[kNP], slot_empty[2];
     uint32_t tmem;
     int abort_flag;
 };
@@ -108,7 +118,8 @@ struct CSmall {
     uint32_t tmem;
     int abort_flag;
 };
-static_assert(sizeof(PSmall) <= kSmallBytes && sizeof(CSmall) <= kSmallBytes, "small blocks");
+static_assert(sizeof(PSmall) <= kPSmallBytes && sizeof(CSmall) <= kCSmallBytes, "small blocks");
+static_assert(kPXs + 32 * kLdX3 * 4 <= kPIn, "A, T and the merge scratch fit the input buffer");
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 
 // consumer TMEM columns (512): W^T then S W^T | U^T | S Q^T x2 | O_intra^T x2 | S
@@ -243,22 +254,19 @@ __device__ __forceinline__ void producer(const GdnArgs &a, const CUtensorMap *tm
     PSmall *s = reinterpret_cast<PSmall *>(sm + kPOffSmall);
     volatile int *abort_flag = &s->abort_flag;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    if (warp >= 8) return;  // two 4-warp pipelines
-    const int p = warp >> 2, quad = warp & 3, t = tid & 127;
+    const int p = warp >> 2, quad = warp & 3, t = tid & 127;   // pipeline p: chunks c = p mod 3
     const uint32_t bar_id = 1 + p;
     uint8_t *in = sm + kPOffIn + p * kPIn;
-    uint8_t *out_base = sm + kPOffOut + p * 2 * kOutBytes;
-    // A and then T = (I + A)^{-1} share one array: every block of A is dead
-    // before the same block of T is written, and A's zero upper triangle is
-    // exactly the zero upper blocks the merges read.
-    float *As = reinterpret_cast<float *>(sm + kPOffAT + p * kPAT);
+    // After the [K;Q] K^T MMA, A and then T = (I + A)^{-1} share the input
+    // buffer: every block of A is dead before the same block of T is written,
+    // and A's zero upper triangle is exactly the zero upper blocks the merges read.
+    float *As = reinterpret_cast<float *>(in);
     float *Ts = As;
-    float *Xs = As + kC * kLdA;
+    float *Xs = reinterpret_cast<float *>(in + kPXs);
 
     const uint32_t tcol = tbase + p * 64;            // [K;Q] K^T
-    const uint32_t r_full =
-        mapa_shared(sm + kCOffSmall + offsetof(CSmall, full) + p * sizeof(uint64_t), 1);
-    const uint32_t r_slot = mapa_shared(sm + p * kSlotBytes, 1);
+    const uint32_t r_full0 = mapa_shared(sm + kCOffSmall + offsetof(CSmall, full), 1);
+    const uint32_t r_slot0 = mapa_shared(sm, 1);
     float amax = 0.f;
 
     auto issue_in = [&](int c) {
@@ -288,38 +296,13 @@ __device__ __forceinline__ void producer(const GdnArgs &a, const CUtensorMap *tm
     load_gates(p);
 
     int k = 0;
-    for (int c = p; c < nchunks; c += 2, ++k) {
+    for (int c = p; c < nchunks; c += kNP, ++k) {
         const int nc = (int)min((long)kC, len - (long)c * kC);
-        // Two outgoing buffers per pipeline: by the time a buffer is rewritten
-        // (this pipeline's chunk c - 4), the consumer has finished chunk c - 4,
-        // so the bulk copy out of it is long complete.
-        uint8_t *out = out_base + (k & 1) * kOutBytes;
-        float *gout = reinterpret_cast<float *>(out + kOutG);
-
-        // decay: g = inclusive cumulative sum of log alpha (padding adds 0)
-        const float la = la_next, bt = b_next, et = e_next;
-        load_gates(c + 2);
-        if (t < kC) {
-            float x = la;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const float y = __shfl_up_sync(0xffffffffu, x, o);
-                if (lane >= o) x += y;
-            }
-            s->scan[p][t] = x;
-            s->beta[p][t] = bt;
-            s->eta[p][t] = et;
-        }
-        named_sync(bar_id, 128);
-        if (t < kC) gout[t] = s->scan[p][t] + (t >= 32 ? s->scan[p][31] : 0.f);
-        named_sync(bar_id, 128);
-        const float gC = gout[kC - 1];
-        if (t < kC) {
-            gout[kC + t] = __expf(gout[t]);
-            gout[2 * kC + t] = __expf(gC - gout[t]);
-            s->colf[p][t] = __expf(gout[31] - gout[t]);
-            s->colb[p][t] = s->beta[p][t] * gout[kC + t];  // beta e^g
-        }
+        // Outgoing buffer c % 5 last held chunk c - 5.  Before starting chunk
+        // c this pipeline shipped chunk c - 3, after the consumer had released
+        // the ring slot of chunk c - 5, so that copy had landed long before.
+        uint8_t *out = sm + kPOffOut + (c % kNOut) * kOutG;
+        float *gout = s->g[c % kNOut];
 
         // q/k tiles (bf16: K K^T and Q K^T are exact products); rows past the
         // sequence are zeroed (they may hold another sequence)
@@ -335,7 +318,8 @@ __device__ __forceinline__ void producer(const GdnArgs &a, const CUtensorMap *tm
         tc_fence_before();
         named_sync(bar_id, 128);
 
-        // [K;Q] K^T: lanes 0-63 K K^T, lanes 64-127 Q K^T
+        // [K;Q] K^T: lanes 0-63 K K^T, lanes 64-127 Q K^T; the decay vectors
+        // below are computed while it runs
         if (t == 0) {
             tc_fence_after();
             const uint32_t id = idesc_bf16_f32(128, 64, 0, 0);
@@ -347,6 +331,35 @@ __device__ __forceinline__ void producer(const GdnArgs &a, const CUtensorMap *tm
             }
             mma_commit(&s->mma[p]);
         }
+
+        // decay: g = inclusive cumulative sum of log alpha (padding adds 0),
+        // from the two warp scans; every thread forms g_31 and g_C itself
+        const float la = la_next, bt = b_next, et = e_next;
+        load_gates(c + kNP);
+        if (t < kC) {
+            float x = la;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float y = __shfl_up_sync(0xffffffffu, x, o);
+                if (lane >= o) x += y;
+            }
+            s->scan[p][t] = x;
+            s->beta[p][t] = bt;
+            s->eta[p][t] = et;
+        }
+        named_sync(bar_id, 128);
+        const float g31 = s->scan[p][31];
+        const float gC = g31 + s->scan[p][kC - 1];
+        if (t < kC) {
+            const float gt = s->scan[p][t] + (t >= 32 ? g31 : 0.f);
+            const float egt = __expf(gt);
+            gout[t] = gt;
+            gout[kC + t] = egt;
+            gout[2 * kC + t] = __expf(gC - gt);
+            s->colf[p][t] = __expf(g31 - gt);
+            s->colb[p][t] = bt * egt;  // beta e^g
+        }
+        named_sync(bar_id, 128);
         wait_bar(&s->mma[p], k & 1, false, abort_flag, a.status);
         tc_fence_after();
 
@@ -355,71 +368,55 @@ __device__ __forceinline__ void producer(const GdnArgs &a, const CUtensorMap *tm
         // of the chunk (g_r = g_31), so each entry costs two multiplies; if the
         // chunk's total decay could push a factor out of fp32 range, every entry
         // is exponentiated on its own instead.  Columns past the diagonal are 0.
+        // The loop runs over groups of 8 columns and is not unrolled: this code
+        // runs once per chunk, and a compact body stays in the instruction cache.
         {
             const bool is_k = t < kC;
             const int i = is_k ? t : t - kC;
             const float gi = gout[i], bi = s->beta[p][i];
             const float gr = gout[31];
             const bool split = (gout[0] - gC) < 80.f;  // uniform across the CTA
-            const float rowf = (is_k ? bi : 1.f) * (split ? __expf(gi - gr) : 1.f);
+            const float base = is_k ? bi : 1.f;
+            const float rowf = base * (split ? __expf(gi - gr) : 1.f);
             const float *colf = s->colf[p];
-            float x[32];
-            #pragma unroll 1
-            for (int half = 0; half < 2; ++half) {
-                if (half == 1 && quad % 2 == 0) {  // rows 0-31 of A / P: all j >= 32 are zero
-                    if (is_k) {
-#pragma unroll
-                        for (int q = 0; q < 8; ++q)
-                            *reinterpret_cast<float4 *>(As + i * kLdA + 32 + 4 * q) =
-                                make_float4(0.f, 0.f, 0.f, 0.f);
-                    } else {
-#pragma unroll
-                        for (int jj = 0; jj < 32; ++jj) x[jj] = 0.f;
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) st_chunk(out + kOutP, i, 4 + q, x + q * 8, &amax);
-                    }
-                    continue;
-                }
-                tmem_ld32(lane_addr(tcol, quad, half * 32), x);
-                tmem_ld_wait();
-                if (split) {
-#pragma unroll
-                    for (int jj = 0; jj < 32; ++jj) {
-                        const int j = half * 32 + jj;
-                        const bool keep = is_k ? (j < i) : (j <= i);
-                        x[jj] = keep ? x[jj] * (rowf * colf[j]) : 0.f;
-                    }
-                } else {  // extreme in-chunk decay: exponentiate each entry
-                    const float base = is_k ? bi : 1.f;
 #pragma unroll 1
-                    for (int jj = 0; jj < 32; ++jj) {
-                        const int j = half * 32 + jj;
-                        const bool keep = is_k ? (j < i) : (j <= i);
-                        const float d = base * __expf(gi - gout[j]);
-                        float v = 0.f;
+            for (int grp = 0; grp < 8; ++grp) {
+                float y[8];
+                if (grp >= 4 && quad % 2 == 0) {  // rows 0-31 of A / P: all j >= 32 are zero
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) v = (e == jj) ? x[e] : v;
-                        v = keep ? v * d : 0.f;
+                    for (int e = 0; e < 8; ++e) y[e] = 0.f;
+                } else {
+                    tmem_ld8(lane_addr(tcol, quad, grp * 8), y);
+                    const float4 c0 = *reinterpret_cast<const float4 *>(colf + grp * 8);
+                    const float4 c1 = *reinterpret_cast<const float4 *>(colf + grp * 8 + 4);
+                    const float cf[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+                    tmem_ld_wait();
+                    if (split) {
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) x[e] = (e == jj) ? v : x[e];
+                        for (int e = 0; e < 8; ++e) {
+                            const int j = grp * 8 + e;
+                            const bool keep = is_k ? (j < i) : (j <= i);
+                            y[e] = keep ? y[e] * (rowf * cf[e]) : 0.f;
+                        }
+                    } else {  // extreme in-chunk decay: exponentiate each entry
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            const int j = grp * 8 + e;
+                            const bool keep = is_k ? (j < i) : (j <= i);
+                            y[e] = keep ? y[e] * (base * __expf(gi - gout[j])) : 0.f;
+                        }
                     }
                 }
                 if (is_k) {
-#pragma unroll
-                    for (int q = 0; q < 8; ++q)
-                        *reinterpret_cast<float4 *>(As + i * kLdA + half * 32 + 4 * q) =
-                            make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
+                    float *dst = As + i * kLdA + grp * 8;
+                    *reinterpret_cast<float4 *>(dst) = make_float4(y[0], y[1], y[2], y[3]);
+                    *reinterpret_cast<float4 *>(dst + 4) = make_float4(y[4], y[5], y[6], y[7]);
                 } else {
-#pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        st_chunk(out + kOutP, i, half * 4 + q, x + q * 8, &amax);
+                    st_chunk(out + kOutP, i, grp, y, &amax);
                 }
             }
         }
-        tc_fence_before();
         named_sync(bar_id, 128);
-        // the q/k buffer is free (its MMA is done): fetch the next chunk
-        if (t == 0 && c + 2 < nchunks && !*abort_flag) issue_in(c + 2);
 
         // T = (I + A)^{-1}
         // (1) 16x16 diagonal blocks: warp `quad` owns block `quad`, lane l < 16
@@ -533,12 +530,28 @@ __device__ __forceinline__ void producer(const GdnArgs &a, const CUtensorMap *tm
         fence_async_smem();
         named_sync(bar_id, 128);
 
-        // ship P, T', T'' and the decay vectors once the consumer's slot is free
         if (t == 0) {
-            if (wait_bar(&s->slot_empty[p], (k + 1) & 1, true, abort_flag, a.status)) {
-                mbar_arrive_expect_tx_remote(r_full, kOutBytes);
-                bulk_copy_to_peer(r_slot, out, kOutBytes, r_full);
+            // A and T are dead: the input buffer takes this pipeline's next chunk
+            if (c + kNP < nchunks && !*abort_flag) issue_in(c + kNP);
+            // Ship P, T', T'' and the decay vectors into ring slot c & 1, in
+            // chunk order: after chunk c - 1 has been shipped (by pipeline
+            // (c - 1) % 3, its ((c - 1) / 3)-th chunk), and once the consumer
+            // has released the slot's previous chunk c - 2.  In order, every
+            // parity below is at most one phase from the one awaited.
+            bool ok = true;
+            if (c > 0)
+                ok = wait_bar(&s->shipped[(c - 1) % kNP], ((c - 1) / kNP) & 1, false, abort_flag,
+                              a.status);
+            ok = ok && wait_bar(&s->slot_empty[c & 1], ((c >> 1) + 1) & 1, true, abort_flag,
+                                a.status);
+            if (ok) {
+                const uint32_t r_full = r_full0 + (c & 1) * sizeof(uint64_t);
+                const uint32_t r_slot = r_slot0 + (c & 1) * kSlotBytes;
+                mbar_arrive_expect_tx_remote(r_full, kOutG + kGBytes);
+                bulk_copy_to_peer(r_slot, out, kOutG, r_full);
+                bulk_copy_to_peer(r_slot + kOutG, gout, kGBytes, r_full);
             }
+            mbar_arrive(&s->shipped[p]);
         }
     }
     if (amax > kF16Max) atomicOr(a.status, 0x4u);
@@ -887,16 +900,17 @@ gdn_tc_kernel(const GdnArgs a, const __grid_constant__ CUtensorMap tm_q,
     const int nchunks = (int)((len + kC - 1) / kC);
 
     uint32_t *tmem_slot;
-    const uint32_t ncols = rank == 0 ? 128 : 512;
+    const uint32_t ncols = rank == 0 ? 256 : 512;  // producer: 64 columns per pipeline
     if (rank == 0) {
         PSmall *s = reinterpret_cast<PSmall *>(sm + kPOffSmall);
         tmem_slot = &s->tmem;
         if (tid == 0) {
-            for (int i = 0; i < 2; ++i) {
+            for (int i = 0; i < kNP; ++i) {
                 mbar_init(&s->tma_in[i], 1);
                 mbar_init(&s->mma[i], 1);
-                mbar_init(&s->slot_empty[i], 1);
+                mbar_init(&s->shipped[i], 1);
             }
+            for (int i = 0; i < 2; ++i) mbar_init(&s->slot_empty[i], 1);
             s->abort_flag = 0;
             fence_mbar_init();
             prefetch_tensormap(&tm_q);
