@@ -30,11 +30,11 @@
 //    consumer's mbarrier.
 //  * rank 1, the consumer, keeps the state slice (128 x 128 fp32) in TMEM for
 //    the whole walk and loads its own q/k/v tiles by TMA.  Warps 0-3 run the
-//    state chain (fp16 copy of S, S W^T and S Q^T, V_new, V_new^T P^T and the
-//    state update) and issue the next chunk's W^T and U^T one chunk ahead;
+//    state chain (fp16 copy of S, S W^T and S Q^T, V_new, the state update
+//    and V_new^T P^T) and issue the next chunk's W^T and U^T one chunk ahead;
 //    warps 4-7 convert the q/k/v tiles to fp16 and read W^T out of TMEM into
-//    its operand tile; warps 8-11 write the outputs (TMA bulk tensor stores
-//    for full chunks).
+//    its operand tile; warps 8-11 write the outputs (through a small staging
+//    tile, 16 bytes per store).
 //
 // Every MMA has M = 128, so a result row is one TMEM lane and one epilogue
 // thread.  Operands are fp16 (11-bit significand; bf16 operands would leave
@@ -97,7 +97,8 @@ constexpr int kPOffSmall = kPOffOut + kNOut * kOutG;
 constexpr int kCOffW = 2 * kSlotBytes;             // W^T rows d (MN-major B operand), fp16
 constexpr int kCOffSb = kCOffW + 16384;            // S as fp16, 2 d_k halves x 128 rows
 constexpr int kCOffVnT = kCOffSb + 32768;          // V_new^T rows v (K-major), fp16
-constexpr int kCOffSmall = kCOffVnT + 16384;
+constexpr int kCOffStage = kCOffVnT + 16384;       // outputs of 32 tokens, 2 x [32][64] bf16
+constexpr int kCOffSmall = kCOffStage + 8192;
 constexpr int kCSmallBytes = 3072;
 constexpr int kPSmallBytes = 8192;
 constexpr int kSmemBytes = (kCOffSmall + kCSmallBytes > kPOffSmall + kPSmallBytes
@@ -114,7 +115,7 @@ struct PSmall {
 struct CSmall {
     float egc[2][kC];
     uint64_t full[2], tma[2], conv[2], egc_full[2], w_mma, w_ready, mma1, mma2, out_full[2],
-        out_done[2];
+        out_done[2], sq_done[2];
     uint32_t tmem;
     int abort_flag;
 };
@@ -240,6 +241,9 @@ __device__ __noinline__ bool wait_cluster(uint64_t *bar, uint32_t parity, volati
 __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, bool cluster_scope,
                                          volatile int *abort_flag, unsigned int *status)
 {
+    // inline non-blocking probe first: most waits find their phase complete
+    if (cluster_scope ? mbar_test_wait_cluster(bar, parity) : mbar_test_wait(bar, parity))
+        return true;
     return cluster_scope ? wait_cluster(bar, parity, abort_flag, status)
                          : wait_cta(bar, parity, abort_flag, status);
 }
@@ -562,7 +566,6 @@ __device__ __forceinline__ void producer(const GdnArgs &a, const CUtensorMap *tm
 // ======================================================================
 __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm_q,
                                          const CUtensorMap *tm_k, const CUtensorMap *tm_v,
-                                         const CUtensorMap *tm_o,
                                          uint8_t *sm, uint32_t tbase, long start, long len,
                                          int nchunks, int h, int n, int v0)
 {
@@ -571,7 +574,7 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
     const int tid = threadIdx.x, warp = tid >> 5;
     const int quad = warp & 3;
     const int H = a.H, dv = a.dv;
-    uint8_t *Sb = sm + kCOffSb, *VnT = sm + kCOffVnT, *Wt = sm + kCOffW;
+    uint8_t *Sb = sm + kCOffSb, *VnT = sm + kCOffVnT, *Wt = sm + kCOffW, *stage = sm + kCOffStage;
     const uint32_t r_slot_empty = mapa_shared(sm + kPOffSmall + offsetof(PSmall, slot_empty), 0);
     float amax = 0.f;
 
@@ -639,6 +642,8 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
             wait_bar(&s->full[sl], kk & 1, true, abort_flag, a.status);
             wait_bar(&s->conv[sl], kk & 1, false, abort_flag, a.status);
             wait_bar(&s->out_done[sl], (kk + 1) & 1, false, abort_flag, a.status);
+            if (c > 0)  // S Q^T of chunk c - 1 (another thread's MMAs) has read the fp16 S copy
+                wait_bar(&s->sq_done[sl ^ 1], ((c - 1) >> 1) & 1, false, abort_flag, a.status);
             if (t < kC) {
                 s->egc[sl][t] = gs[kC + t];
                 mbar_arrive(&s->egc_full[sl]);
@@ -673,24 +678,31 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
             fence_async_smem();
             tc_fence_before();
             named_sync(1, 128);
+            if (t == 32) {  // S Q^T (for the outputs) from a second thread while S W^T runs
+                tc_fence_after();
+                const uint32_t id_q = idesc_f16_f32(128, 64, 0, 0);
+                const uint64_t ds = sdesc_sw128(smem_u32(Sb), 16, 1024);
+                const uint64_t dq = sdesc_sw128(smem_u32(slot) + kSlotKQ + 8192, 16, 1024);
+                const uint32_t csq = tbase + kColSQ + sl * 64;
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    const uint32_t o = ((ks >> 2) * 16384 + (ks & 3) * 32) >> 4;
+                    mma_f16kind(csq, ds + o, dq + o, id_q, ks > 0);
+                }
+                mma_commit(&s->sq_done[sl]);
+            }
 
-            // S W^T;  S Q^T  (W^T rows written by warps 4-7)
+            // S W^T (W^T rows written by warps 4-7)
             wait_bar(&s->w_ready, c & 1, false, abort_flag, a.status);
             if (t == 0) {
                 tc_fence_after();
                 const uint32_t id_w = idesc_f16_f32(128, 64, 0, 1);
-                const uint32_t id_q = idesc_f16_f32(128, 64, 0, 0);
-                const uint32_t sa = smem_u32(slot);
                 const uint64_t ds = sdesc_sw128(smem_u32(Sb), 16, 1024);
                 const uint64_t dw = sdesc_sw128(smem_u32(Wt), 8192, 1024);
-                const uint64_t dq = sdesc_sw128(sa + kSlotKQ + 8192, 16, 1024);
-                const uint32_t csq = tbase + kColSQ + sl * 64;
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
                     const uint32_t oa = ((ks >> 2) * 16384 + (ks & 3) * 32) >> 4;
-                    const uint32_t oq = oa;
                     mma_f16kind(tbase + kColSW, ds + oa, dw + ks * (2048 >> 4), id_w, ks > 0);
-                    mma_f16kind(csq, ds + oa, dq + oq, id_q, ks > 0);
                 }
                 mma_commit(&s->mma1);
             }
@@ -721,7 +733,8 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
             tc_fence_before();
             named_sync(1, 128);
 
-            // O_intra^T = V_new^T P^T;  S += (V_new e^{g_C-g})^T K
+            // S += (V_new e^{g_C-g})^T K first (the chain waits for it), then
+            // O_intra^T = V_new^T P^T
             if (t == 0) {
                 tc_fence_after();
                 const uint32_t ido = idesc_f16_f32(128, 64, 0, 0);
@@ -733,19 +746,23 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
                 const uint64_t dk = sdesc_sw128(sa + kSlotKQ, 16384, 1024);
                 const uint32_t co = tbase + kColO + sl * 64;
 #pragma unroll
-                for (int ks = 0; ks < 4; ++ks) {
-                    mma_f16kind(co, dvn + ks * (32 >> 4), dp + ks * (32 >> 4), ido, ks > 0);
+                for (int ks = 0; ks < 4; ++ks)
                     mma_f16kind(tbase + kColS, dvs + ks * (32 >> 4), dk + ks * (2048 >> 4), ids, 1);
-                }
                 mma_commit(&s->mma2);
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
+                    mma_f16kind(co, dvn + ks * (32 >> 4), dp + ks * (32 >> 4), ido, ks > 0);
                 mma_commit(&s->out_full[sl]);
             }
             wait_bar(&s->mma2, c & 1, false, abort_flag, a.status);
             tc_fence_after();
-            // slot consumed: hand it back to the producer, refill our tiles
-            // our q/k/v tiles are consumed: refill them (the shipped part of
-            // the slot is handed back by warps 4-7 once the outputs are out)
-            if (t == 0 && c + 2 < nchunks && !*abort_flag) issue_qkv(c + 2);
+            // our q/k/v tiles are consumed once S Q^T (output warps) is done too:
+            // refill them (the shipped part of the slot is handed back by warps
+            // 8-11 once the outputs are out)
+            if (t == 0 && c + 2 < nchunks && !*abort_flag) {
+                wait_bar(&s->sq_done[sl], kk & 1, false, abort_flag, a.status);
+                issue_qkv(c + 2);
+            }
             if (c + 1 < nchunks) {  // next chunk's W^T, U^T (their columns are free now)
                 wait_bar(&s->full[sl ^ 1], ((c + 1) >> 1) & 1, true, abort_flag, a.status);
                 wait_bar(&s->conv[sl ^ 1], ((c + 1) >> 1) & 1, false, abort_flag, a.status);
@@ -789,22 +806,23 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
             fence_async_smem();
             mbar_arrive(&s->conv[sl]);
         };
-        // o_i = e^{g_i} (S Q^T)_i + O_intra,i.  A full chunk is staged as a
-        // [64 tokens][128 d_v] bf16 tile in the slot's P|T' region (free once
-        // the chunk's second MMA batch is done) and written with two TMA
-        // stores; a partial chunk (the end of a sequence) uses plain stores so
-        // nothing lands in the next sequence.  The slot goes back to the
-        // producer after that.
+        // o_i = e^{g_i} (S Q^T)_i + O_intra,i.  The slot's shipped part goes
+        // back to the producer first: O_intra, the last reader of P, has
+        // completed.  A full chunk is written 32 tokens at a time through an
+        // 8 KB staging tile ([32 tokens][128 d_v] bf16 as two 128-byte-swizzled
+        // boxes) and two TMA stores; a partial chunk (the end of a sequence)
+        // uses plain stores so nothing lands in the next sequence.
         auto output = [&](int c) {
             const int sl = c & 1;
-            uint8_t *slot = sm + sl * kSlotBytes;
             const int nc = (int)min((long)kC, len - (long)c * kC);
             const long tok0 = start + (long)c * kC;
             wait_bar(&s->egc_full[sl], (c >> 1) & 1, false, abort_flag, a.status);
             wait_bar(&s->out_full[sl], (c >> 1) & 1, false, abort_flag, a.status);
+            wait_bar(&s->sq_done[sl], (c >> 1) & 1, false, abort_flag, a.status);
             tc_fence_after();
+            if (t == 0) mbar_arrive_remote(r_slot_empty + sl * sizeof(uint64_t));
             const size_t col = (size_t)v0 + t;
-            uint8_t *stage = slot + kOutP + (t >> 6) * 8192;  // d_v half of this thread
+            uint8_t *box = stage + (t >> 6) * 4096;  // d_v half of this thread
             const int vc = (t & 63) >> 3, ve = t & 7;
             float x[32], y[32];
 #pragma unroll 1
@@ -814,11 +832,22 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
                 tmem_ld_wait();
                 if (nc == kC) {
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const int i = half * 32 + j;
-                        reinterpret_cast<__nv_bfloat16 *>(stage + sw128(i, vc))[ve] =
-                            __float2bfloat16_rn(fmaf(s->egc[sl][i], x[j], y[j]));
+                    for (int j = 0; j < 32; ++j)
+                        reinterpret_cast<__nv_bfloat16 *>(box + sw128(j, vc))[ve] =
+                            __float2bfloat16_rn(fmaf(s->egc[sl][half * 32 + j], x[j], y[j]));
+                    named_sync(3, 128);
+                    // copy out: 16 bytes (8 d_v columns of one token) per thread
+                    // and step, 16 threads per 256-byte token row
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) {
+                        const int idx = t + 128 * r, j = idx >> 4, cc = idx & 15;
+                        const uint4 u = *reinterpret_cast<const uint4 *>(
+                            stage + (cc >> 3) * 4096 + sw128(j, cc & 7));
+                        if (v0 + 8 * cc < dv)
+                            *reinterpret_cast<uint4 *>(
+                                o + ((size_t)(tok0 + half * 32 + j) * H + h) * dv + v0 + 8 * cc) = u;
                     }
+                    named_sync(3, 128);  // the staging tile is free again
                 } else if (col < (size_t)dv) {
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
@@ -831,17 +860,6 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
             }
             tc_fence_before();
             mbar_arrive(&s->out_done[sl]);
-            if (nc == kC) {
-                fence_async_smem();
-                named_sync(3, 128);
-                if (t == 0) {  // the store clips columns past d_v; a box wholly past it is skipped
-                    tma_store_3d(tm_o, slot + kOutP, v0, h, (int)tok0);
-                    if (v0 + 64 < dv) tma_store_3d(tm_o, slot + kOutP + 8192, v0 + 64, h, (int)tok0);
-                    bulk_commit();
-                    bulk_wait_read();
-                }
-            }
-            if (t == 0) mbar_arrive_remote(r_slot_empty + sl * sizeof(uint64_t));
         };
         auto w_epilogue = [&](int c) {
             wait_bar(&s->w_mma, c & 1, false, abort_flag, a.status);
@@ -865,7 +883,6 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
             }
         } else {
             for (int c = 0; c < nchunks; ++c) output(c);
-            if (t == 0) bulk_wait_all();
         }
     }
     if (amax > kF16Max) atomicOr(a.status, 0x4u);
@@ -873,8 +890,7 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 gdn_tc_kernel(const GdnArgs a, const __grid_constant__ CUtensorMap tm_q,
-              const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-              const __grid_constant__ CUtensorMap tm_o)
+              const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>(
@@ -930,6 +946,8 @@ gdn_tc_kernel(const GdnArgs a, const __grid_constant__ CUtensorMap tm_q,
             }
             mbar_init(&s->w_mma, 1);
             mbar_init(&s->w_ready, 128);
+            mbar_init(&s->sq_done[0], 1);
+            mbar_init(&s->sq_done[1], 1);
             mbar_init(&s->mma1, 1);
             mbar_init(&s->mma2, 1);
             s->abort_flag = 0;
@@ -937,7 +955,6 @@ gdn_tc_kernel(const GdnArgs a, const __grid_constant__ CUtensorMap tm_q,
             prefetch_tensormap(&tm_q);
             prefetch_tensormap(&tm_k);
             prefetch_tensormap(&tm_v);
-            prefetch_tensormap(&tm_o);
         }
     }
     if (warp == 0) {
@@ -950,7 +967,7 @@ gdn_tc_kernel(const GdnArgs a, const __grid_constant__ CUtensorMap tm_q,
     const uint32_t tbase = *tmem_slot;
 
     if (rank == 0) producer(a, &tm_q, &tm_k, sm, tbase, start, len, nchunks, h);
-    else consumer(a, &tm_q, &tm_k, &tm_v, &tm_o, sm, tbase, start, len, nchunks, h, n, v0);
+    else consumer(a, &tm_q, &tm_k, &tm_v, sm, tbase, start, len, nchunks, h, n, v0);
 
     tc_fence_before();
     __syncthreads();
@@ -1005,15 +1022,15 @@ bool gdn_tc_supported(const GdnArgs &a)
 cudaError_t gdn_launch_tc(const GdnArgs &a, cudaStream_t s, int *launches)
 {
     const long tokens = a.cu_seqlens ? (long)a.T : (long)a.N * a.T;
-    CUtensorMap mq, mk, mv, mo;
+    CUtensorMap mq, mk, mv;
     if (!make_map(&mq, a.q, tokens, a.H, a.dk) || !make_map(&mk, a.k, tokens, a.H, a.dk) ||
-        !make_map(&mv, a.v, tokens, a.H, a.dv) || !make_map(&mo, a.o, tokens, a.H, a.dv))
+        !make_map(&mv, a.v, tokens, a.H, a.dv))
         return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(gdn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          kSmemBytes);
     if (e != cudaSuccess) return e;
     dim3 grid(2 * ((a.dv + kDVT - 1) / kDVT), a.H, a.N);
-    gdn_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(a, mq, mk, mv, mo);
+    gdn_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(a, mq, mk, mv);
     *launches = 1;
     return cudaGetLastError();
 }
