@@ -14,7 +14,7 @@
 //                       T'' = T diag(beta e^g),   T' = T diag(eta)
 //                       (eta, the write strength, is beta unless given)
 //                       W^T = K^T T''^T,          U^T = V^T T'^T
-//   state chain:        V_new^T = U^T - S W^T
+//   state chain:        V_new^T = U^T - S W^T   (accumulated onto U^T with -W^T)
 //                       O^T = e^{g} (S Q^T) + V_new^T P^T
 //                       S <- e^{g_C} S + (V_new * e^{g_C - g})^T K
 //
@@ -123,7 +123,7 @@ static_assert(sizeof(PSmall) <= kPSmallBytes && sizeof(CSmall) <= kCSmallBytes, 
 static_assert(kPXs + 32 * kLdX3 * 4 <= kPIn, "A, T and the merge scratch fit the input buffer");
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 
-// consumer TMEM columns (512): W^T then S W^T | U^T | S Q^T x2 | O_intra^T x2 | S
+// consumer TMEM columns (512): W^T | U^T then V_new^T | S Q^T x2 | O_intra^T x2 | S
 constexpr uint32_t kColSW = 0, kColU = 64, kColSQ = 128, kColO = 256, kColS = 384;
 
 __device__ __forceinline__ uint32_t pack_f16(float a, float b)
@@ -692,7 +692,8 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
                 mma_commit(&s->sq_done[sl]);
             }
 
-            // S W^T (W^T rows written by warps 4-7)
+            // V_new^T = U^T + S (-W^T), accumulated onto U^T (-W^T rows written
+            // by warps 4-7; U^T is complete since w_ready follows the W^T, U^T commit)
             wait_bar(&s->w_ready, c & 1, false, abort_flag, a.status);
             if (t == 0) {
                 tc_fence_after();
@@ -702,28 +703,31 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
                     const uint32_t oa = ((ks >> 2) * 16384 + (ks & 3) * 32) >> 4;
-                    mma_f16kind(tbase + kColSW, ds + oa, dw + ks * (2048 >> 4), id_w, ks > 0);
+                    mma_f16kind(tbase + kColU, ds + oa, dw + ks * (2048 >> 4), id_w, 1);
                 }
                 mma_commit(&s->mma1);
             }
             wait_bar(&s->mma1, c & 1, false, abort_flag, a.status);
             tc_fence_after();
 
-            // V_new^T = U^T - S W^T -> VnT; V_new^T * e^{g_C - g} -> slot V region
+            // V_new^T -> VnT; V_new^T * e^{g_C - g} -> slot V region
             {
                 const float *ekc = gs + 2 * kC;
-                float u[32], w[32];
+                float u[32];
                 #pragma unroll 1
                 for (int half = 0; half < 2; ++half) {
                     tmem_ld32(lane_addr(tbase, quad, kColU + half * 32), u);
-                    tmem_ld32(lane_addr(tbase, quad, kColSW + half * 32), w);
-                    tmem_ld_wait();
+                    float e[32];
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) u[j] -= w[j];
+                    for (int q = 0; q < 8; ++q) {
+                        const float4 f = *reinterpret_cast<const float4 *>(ekc + half * 32 + 4 * q);
+                        e[4 * q] = f.x; e[4 * q + 1] = f.y; e[4 * q + 2] = f.z; e[4 * q + 3] = f.w;
+                    }
+                    tmem_ld_wait();
 #pragma unroll
                     for (int q = 0; q < 4; ++q) st_chunk(VnT, t, half * 4 + q, u + q * 8, &amax);
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) u[j] *= ekc[half * 32 + j];
+                    for (int j = 0; j < 32; ++j) u[j] *= e[j];
 #pragma unroll
                     for (int q = 0; q < 4; ++q)
                         st_chunk(slot + kSlotV, t, half * 4 + q, u + q * 8, &amax);
@@ -869,6 +873,8 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
             for (int half = 0; half < 2; ++half) {
                 tmem_ld32(lane_addr(tbase, quad, kColSW + half * 32), x);
                 tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 32; ++j) x[j] = -x[j];  // -W^T: S (-W^T) accumulates onto U^T
 #pragma unroll
                 for (int q = 0; q < 4; ++q) st_chunk(Wt, t, half * 4 + q, x + q * 8, &amax);
             }
