@@ -112,6 +112,53 @@ def _chunk(q, k, v, log_alpha, beta, eta, S0, o, S_final, C, cu_seqlens, stream,
     return o, S_final
 
 
+def gdn_chunk_fwd_scan(q, k, v, log_alpha, beta, S0=None, o=None, S_final=None, C=64,
+                       segments=0, workspace=None, stream=None):
+    """``gdn_chunk_fwd`` with each sequence cut into ``segments`` pieces that
+    run in parallel (0 = chosen by the library); returns ``(o, S_final)``.
+    ``workspace`` is a uint8 CUDA tensor of at least
+    ``gdn_chunk_fwd_scan_workspace_size(...)`` bytes, allocated here if None."""
+    lib = _lib.load()
+    if q.dtype not in _DTYPES:
+        raise TypeError("q/k/v dtype must be float32 or bfloat16, got %s" % q.dtype)
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _need_cuda(name, t, q.dtype)
+    _need_cuda("log_alpha", log_alpha, torch.float32)
+    _need_cuda("beta", beta, torch.float32)
+    _need_cuda("S0", S0, torch.float32)
+    if q.dim() != 4 or k.shape != q.shape or v.dim() != 4 or v.shape[:3] != q.shape[:3]:
+        raise ValueError("q, k must be [B,T,H,d_k] and v [B,T,H,d_v]")
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    if log_alpha.shape != (B, T, H) or beta.shape != (B, T, H):
+        raise ValueError("log_alpha and beta must be [B,T,H]")
+    if S0 is not None and S0.shape != (B, H, dv, dk):
+        raise ValueError("S0 must be [B,H,d_v,d_k] = %s" % ((B, H, dv, dk),))
+    if o is None:
+        o = torch.empty((B, T, H, dv), dtype=q.dtype, device=q.device)
+    _need_cuda("o", o, q.dtype)
+    if S_final is None:
+        S_final = torch.empty((B, H, dv, dk), dtype=torch.float32, device=q.device)
+    _need_cuda("S_final", S_final, torch.float32)
+    with torch.cuda.device(q.device):
+        need = gdn_chunk_fwd_scan_workspace_size(B, H, T, dk, dv, C, segments)
+        if workspace is None:
+            workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+        _need_cuda("workspace", workspace, torch.uint8)
+        st = lib.gdn_chunk_fwd_scan(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(S0), _ptr(o),
+            _ptr(S_final), B, H, T, dk, dv, int(C), _DTYPES[q.dtype], int(segments),
+            _ptr(workspace), workspace.numel(), ctypes.c_void_p(_stream_handle(stream, q.device)))
+    _lib.check(st)
+    return o, S_final
+
+
+def gdn_chunk_fwd_scan_workspace_size(B, H, T, d_k, d_v, C=64, segments=0):
+    """Bytes of device workspace gdn_chunk_fwd_scan needs (0: none)."""
+    return int(_lib.load().gdn_chunk_fwd_scan_workspace_size(B, H, T, d_k, d_v, int(C),
+                                                              int(segments)))
+
+
 def _stream_handle(stream, device):
     if stream is None:
         return torch.cuda.current_stream(device).cuda_stream
@@ -175,8 +222,9 @@ def gdn_get_device_status(stream=None):
 
 
 def gdn_last_launch_count():
-    """(kernels enqueued by the last gdn_chunk_fwd / gdn_decode_step on this
-    thread, path id: 0 fp32 chunk kernel, 1 tcgen05 chunk kernel, 2 decode)."""
+    """(kernels enqueued by the last gdn_chunk_fwd / gdn_chunk_fwd_scan /
+    gdn_decode_step on this thread, path id: 0 fp32 chunk kernel, 1 tcgen05
+    chunk kernel, 2 decode, 3 chunk-level scan)."""
     path = ctypes.c_int(-1)
     n = _lib.load().gdn_last_launch_count(ctypes.byref(path))
     return n, path.value

@@ -55,10 +55,71 @@ bool overlaps(const void *a, size_t na, const void *b, size_t nb)
 
 bool aligned(const void *p, size_t al) { return (reinterpret_cast<uintptr_t>(p) % al) == 0; }
 
-gdn_status_t chunk_fwd(const void *q, const void *k, const void *v, const float *log_alpha,
-                       const float *beta, const float *eta, const float *S0, void *o,
-                       float *S_final, int B, int H, int T, int d_k, int d_v, int C,
-                       const int32_t *cu_seqlens, gdn_dtype_t dtype, void *stream)
+// Workspace of the chunk-level scan: segment boundaries, the state each
+// segment starts from, the segments' zero-start states (later their final
+// states) and their d_k x d_k transitions.
+struct ScanLayout {
+    size_t cu, sin, bseg, mseg, total;
+};
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+ScanLayout scan_layout(int B, int H, int d_k, int d_v, int P)
+{
+    const size_t nseg = (size_t)B * P;
+    ScanLayout l;
+    l.cu = 0;
+    l.sin = align256((nseg + 1) * sizeof(int32_t));
+    l.bseg = l.sin + align256(nseg * H * d_v * d_k * sizeof(float));
+    l.mseg = l.bseg + align256(nseg * H * d_v * d_k * sizeof(float));
+    l.total = l.mseg + align256(nseg * H * d_k * d_k * sizeof(float));
+    return l;
+}
+
+// Segments per sequence: minimise the modelled time of the propagator pass
+// (d_v tiles + one identity tile per unit) and the forward pass (d_v tiles)
+// over waves of clusters, plus the sequential scan (about half a chunk step
+// per segment).
+int choose_segments(int B, int H, int d_v, int nchunks)
+{
+    int dev = 0, sms = 148;
+    if (cudaGetDevice(&dev) == cudaSuccess)
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const long slots = sms / 2 > 0 ? sms / 2 : 1;  // one 2-CTA cluster per unit and wave
+    const long vt = (d_v + 127) / 128;
+    int best = 1;
+    double best_t = 1e300;
+    for (int P = 1; P <= nchunks && P <= 4096; ++P) {
+        const long per = (nchunks + P - 1) / P;
+        const long w1 = ((long)B * H * P * (vt + 1) + slots - 1) / slots;
+        const long w3 = ((long)B * H * P * vt + slots - 1) / slots;
+        const double t = P == 1 ? (double)((B * H * vt + slots - 1) / slots) * nchunks
+                                : (double)(w1 + w3) * per + 0.5 * P;
+        if (t < best_t) {
+            best_t = t;
+            best = P;
+        }
+    }
+    return best;
+}
+
+// Host checks of a forward-pass call; on success *a describes it (with the
+// device status word) and *nothing is set when there is nothing to compute.
+// Segments per sequence for a request (<= 0: chosen here), with no empty
+// segment: ceil(nchunks / ceil(nchunks / P)).
+int segment_count(int B, int H, int d_v, int nchunks, int segments)
+{
+    int P = segments > 0 ? (segments < nchunks ? segments : nchunks)
+                         : choose_segments(B, H, d_v, nchunks);
+    if (P < 1) P = 1;
+    const int per = (nchunks + P - 1) / P;
+    return (nchunks + per - 1) / per;
+}
+
+gdn_status_t check_chunk(const void *q, const void *k, const void *v, const float *log_alpha,
+                         const float *beta, const float *eta, const float *S0, void *o,
+                         float *S_final, int B, int H, int T, int d_k, int d_v, int C,
+                         const int32_t *cu_seqlens, gdn_dtype_t dtype, GdnArgs *a, bool *nothing)
 {
     t_msg[0] = '\0';
     if (B < 0 || H < 0 || T < 0)
@@ -103,32 +164,47 @@ gdn_status_t chunk_fwd(const void *q, const void *k, const void *v, const float 
 
     t_launches = 0;
     t_path = -1;
-    if (!any_units) return GDN_OK;
-    if (!work && !S_final) return GDN_OK;  // nothing to compute, nothing to write
+    *nothing = !any_units || (!work && !S_final);  // nothing to compute, nothing to write
+    if (*nothing) return GDN_OK;
+    a->q = q; a->k = k; a->v = v; a->log_alpha = log_alpha; a->beta = beta; a->eta = eta;
+    a->S0 = S0; a->o = o; a->S_final = S_final;
+    a->N = B; a->H = H; a->T = T; a->dk = d_k; a->dv = d_v; a->C = C;
+    a->cu_seqlens = cu_seqlens;
+    a->dtype = dtype == GDN_BF16 ? 1 : 0;
+    a->mode = 0;
+    a->prop_M = nullptr;
+    return status_word(&a->status);
+}
 
-    GdnArgs a;
-    a.q = q; a.k = k; a.v = v; a.log_alpha = log_alpha; a.beta = beta; a.eta = eta; a.S0 = S0;
-    a.o = o; a.S_final = S_final;
-    a.N = B; a.H = H; a.T = T; a.dk = d_k; a.dv = d_v; a.C = C;
-    a.cu_seqlens = cu_seqlens;
-    a.dtype = dtype == GDN_BF16 ? 1 : 0;
-    gdn_status_t st = status_word(&a.status);
-    if (st != GDN_OK) return st;
-
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    int launches = 0;
+gdn_status_t launch_chunk(const GdnArgs &a, cudaStream_t s, int *launches, int *path)
+{
     cudaError_t e;
-    int path;
     if (gdn_tc_supported(a)) {
-        e = gdn_launch_tc(a, s, &launches);
-        path = 1;
+        e = gdn_launch_tc(a, s, launches);
+        *path = 1;
     } else {
-        e = gdn_launch_simt(a, s, &launches);
-        path = 0;
+        e = gdn_launch_simt(a, s, launches);
+        *path = 0;
     }
     if (e != cudaSuccess)
         return fail(GDN_ERR_CUDA, "kernel launch (%s path): %s",
-                    path ? "tcgen05" : "fp32", cudaGetErrorString(e));
+                    *path ? "tcgen05" : "fp32", cudaGetErrorString(e));
+    return GDN_OK;
+}
+
+gdn_status_t chunk_fwd(const void *q, const void *k, const void *v, const float *log_alpha,
+                       const float *beta, const float *eta, const float *S0, void *o,
+                       float *S_final, int B, int H, int T, int d_k, int d_v, int C,
+                       const int32_t *cu_seqlens, gdn_dtype_t dtype, void *stream)
+{
+    GdnArgs a;
+    bool nothing = false;
+    gdn_status_t st = check_chunk(q, k, v, log_alpha, beta, eta, S0, o, S_final, B, H, T, d_k, d_v,
+                                  C, cu_seqlens, dtype, &a, &nothing);
+    if (st != GDN_OK || nothing) return st;
+    int launches = 0, path = -1;
+    st = launch_chunk(a, static_cast<cudaStream_t>(stream), &launches, &path);
+    if (st != GDN_OK) return st;
     t_launches = launches;
     t_path = path;
     return GDN_OK;
@@ -190,6 +266,106 @@ gdn_status_t gdn_chunk_fwd_eta(const void *q, const void *k, const void *v,
     }
     return chunk_fwd(q, k, v, log_alpha, beta, eta, S0, o, S_final, B, H, T, d_k, d_v, C,
                      cu_seqlens, dtype, stream);
+}
+
+size_t gdn_chunk_fwd_scan_workspace_size(int B, int H, int T, int d_k, int d_v, int C,
+                                         int segments)
+{
+    if (B <= 0 || H <= 0 || T <= 0 || d_k <= 0 || d_v <= 0 || (C != 16 && C != 32 && C != 64))
+        return 0;
+    const int P = segment_count(B, H, d_v, (T + C - 1) / C, segments);
+    return P <= 1 ? 0 : scan_layout(B, H, d_k, d_v, P).total;
+}
+
+gdn_status_t gdn_chunk_fwd_scan(const void *q, const void *k, const void *v,
+                                const float *log_alpha, const float *beta,
+                                const float *S0, void *o, float *S_final,
+                                int B, int H, int T, int d_k, int d_v, int C,
+                                gdn_dtype_t dtype, int segments,
+                                void *workspace, size_t workspace_bytes, void *stream)
+{
+    GdnArgs a;
+    bool nothing = false;
+    gdn_status_t st = check_chunk(q, k, v, log_alpha, beta, nullptr, S0, o, S_final, B, H, T, d_k,
+                                  d_v, C, nullptr, dtype, &a, &nothing);
+    if (st != GDN_OK || nothing) return st;
+    if (!gdn_tc_supported(a))
+        return fail(GDN_ERR_UNSUPPORTED,
+                    "the chunk-level scan runs on the tensor-core kernel: bf16, C = 64 and d_k, d_v "
+                    "multiples of 8 (got dtype %d, d_k=%d, d_v=%d, C=%d)", (int)dtype, d_k, d_v, C);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int nchunks = (T + C - 1) / C;
+    const int P = segment_count(B, H, d_v, nchunks, segments);
+    int launches = 0, path = -1;
+    if (P <= 1) {  // one segment per sequence: the plain forward pass
+        st = launch_chunk(a, s, &launches, &path);
+        if (st != GDN_OK) return st;
+        t_launches = launches;
+        t_path = path;
+        return GDN_OK;
+    }
+    const ScanLayout l = scan_layout(B, H, d_k, d_v, P);
+    if (!workspace || workspace_bytes < l.total)
+        return fail(GDN_ERR_INVALID_ARG, "workspace of %zu bytes needed (%zu given)", l.total,
+                    workspace ? workspace_bytes : (size_t)0);
+    if (!aligned(workspace, 256))
+        return fail(GDN_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+    const size_t tokens = (size_t)B * T;
+    const size_t nqk = tokens * H * d_k * 2, nv = tokens * H * d_v * 2;
+    const size_t ng = tokens * H * sizeof(float), ns = (size_t)B * H * d_v * d_k * sizeof(float);
+    if (overlaps(workspace, l.total, q, nqk) || overlaps(workspace, l.total, k, nqk) ||
+        overlaps(workspace, l.total, v, nv) || overlaps(workspace, l.total, o, nv) ||
+        overlaps(workspace, l.total, log_alpha, ng) || overlaps(workspace, l.total, beta, ng) ||
+        overlaps(workspace, l.total, S0, ns) || overlaps(workspace, l.total, S_final, ns))
+        return fail(GDN_ERR_INVALID_ARG, "workspace overlaps an argument");
+
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    int32_t *cu = reinterpret_cast<int32_t *>(ws + l.cu);
+    float *Sin = reinterpret_cast<float *>(ws + l.sin);
+    float *Bseg = reinterpret_cast<float *>(ws + l.bseg);
+    float *Mseg = reinterpret_cast<float *>(ws + l.mseg);
+    const int per = (nchunks + P - 1) / P;  // chunks per segment
+
+    // (1) segment boundaries, as packed sequences over the B * T token rows
+    cudaError_t e = gdn_launch_segments(cu, B, P, T, per * C, s);
+    if (e != cudaSuccess) return fail(GDN_ERR_CUDA, "segment boundaries: %s", cudaGetErrorString(e));
+    // (2) propagators: per segment, the state reached from zero and the transition
+    GdnArgs pa = a;
+    pa.N = B * P;
+    pa.T = (int)tokens;
+    pa.cu_seqlens = cu;
+    pa.S0 = nullptr;
+    pa.S_final = Bseg;
+    pa.mode = 1;
+    pa.prop_M = Mseg;
+    int n = 0;
+    e = gdn_launch_tc(pa, s, &n);
+    if (e != cudaSuccess) return fail(GDN_ERR_CUDA, "propagator pass: %s", cudaGetErrorString(e));
+    // (3) the state each segment starts from
+    e = gdn_launch_scan(S0, Bseg, Mseg, Sin, B, P, H, d_v, d_k, s);
+    if (e != cudaSuccess) return fail(GDN_ERR_CUDA, "segment scan: %s", cudaGetErrorString(e));
+    // (4) the forward pass of every segment from its own start state
+    GdnArgs fa = pa;
+    fa.S0 = Sin;
+    fa.S_final = Bseg;  // the segments' final states (the zero-start states are consumed)
+    fa.mode = 0;
+    fa.prop_M = nullptr;
+    e = gdn_launch_tc(fa, s, &n);
+    if (e != cudaSuccess) return fail(GDN_ERR_CUDA, "segment forward pass: %s", cudaGetErrorString(e));
+    // (5) each sequence's final state is its last segment's
+    if (S_final) {
+        const size_t per_seq = (size_t)H * d_v * d_k * sizeof(float);
+        for (int b = 0; b < B; ++b) {
+            e = cudaMemcpyAsync(reinterpret_cast<uint8_t *>(S_final) + b * per_seq,
+                                reinterpret_cast<uint8_t *>(Bseg) + ((size_t)b * P + P - 1) * per_seq,
+                                per_seq, cudaMemcpyDeviceToDevice, s);
+            if (e != cudaSuccess)
+                return fail(GDN_ERR_CUDA, "final state copy: %s", cudaGetErrorString(e));
+        }
+    }
+    t_launches = 4;
+    t_path = 3;
+    return GDN_OK;
 }
 
 gdn_status_t gdn_decode_step(const void *q, const void *k, const void *v,

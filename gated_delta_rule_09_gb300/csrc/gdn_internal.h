@@ -16,6 +16,12 @@ struct GdnArgs {
     const int32_t *cu_seqlens;   // device [N + 1] or null
     int dtype;                   // 0 = fp32, 1 = bf16
     unsigned int *status;        // device status word (GDN_DEV_* bits)
+    // 0: the forward pass.  1: segment propagators for the chunk-level scan
+    // (tcgen05 kernel only): per sequence, the state reached from zero (into
+    // S_final) and the d_k x d_k transition M of S_end = S_start M + that
+    // state (into prop_M, [N, H, dk, dk]); no outputs are written.
+    int mode;
+    float *prop_M;
 };
 
 // fp32 CUDA-core kernel: every supported shape and dtype.
@@ -39,3 +45,9 @@ struct GdnDecodeArgs {
 
 // Recurrent (token-by-token) kernel for decoding, on CUDA cores.
 cudaError_t gdn_launch_decode(const GdnDecodeArgs &a, cudaStream_t s, int *launches);
+
+// Chunk-level scan over segments: x_{s+1} = x_s M_s + B_s (fp32, CUDA cores).
+cudaError_t gdn_launch_scan(const float *S0, const float *Bseg, const float *Mseg, float *Sin,
+                            int B, int P, int H, int dv, int dk, cudaStream_t s);
+// Segment boundaries of B equal-length sequences: cu[b * P + j] = b * T + min(j * seg, T).
+cudaError_t gdn_launch_segments(int32_t *cu, int B, int P, int T, int seg_tokens, cudaStream_t s);

@@ -567,7 +567,8 @@ __device__ __forceinline__ void producer(const GdnArgs &a, const CUtensorMap *tm
 __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm_q,
                                          const CUtensorMap *tm_k, const CUtensorMap *tm_v,
                                          uint8_t *sm, uint32_t tbase, long start, long len,
-                                         int nchunks, int h, int n, int v0)
+                                         int nchunks, int h, int n, int v0,
+                                         bool prop, bool is_m)
 {
     CSmall *s = reinterpret_cast<CSmall *>(sm + kCOffSmall);
     volatile int *abort_flag = &s->abort_flag;
@@ -581,11 +582,11 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
     auto issue_qkv = [&](int c) {
         uint8_t *slot = sm + (c & 1) * kSlotBytes;
         const int z = (int)(start + (long)c * kC);
-        mbar_arrive_expect_tx(&s->tma[c & 1], 6 * 8192);
+        mbar_arrive_expect_tx(&s->tma[c & 1], (is_m ? 4 : 6) * 8192);
         for (int b = 0; b < 2; ++b) {
             tma_load_3d(slot + kSlotKQ + b * 16384, tm_k, &s->tma[c & 1], b * 64, h, z);
             tma_load_3d(slot + kSlotKQ + b * 16384 + 8192, tm_q, &s->tma[c & 1], b * 64, h, z);
-            tma_load_3d(slot + kSlotV + b * 8192, tm_v, &s->tma[c & 1], v0 + b * 64, h, z);
+            if (!is_m) tma_load_3d(slot + kSlotV + b * 8192, tm_v, &s->tma[c & 1], v0 + b * 64, h, z);
         }
     };
 
@@ -596,14 +597,18 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
             if (nchunks > 0) issue_qkv(0);
             if (nchunks > 1) issue_qkv(1);
         }
-        {   // initial state -> TMEM; padding rows and columns stay zero
+        {   // initial state -> TMEM; padding rows and columns stay zero.  A
+            // propagator starts from zero, its identity rows from I.
             const int dk = a.dk;
-            const float *src = a.S0 && v0 + t < dv ? a.S0 + (((size_t)n * H + h) * dv + v0 + t) * dk
-                                                   : nullptr;
+            const float *src = !prop && a.S0 && v0 + t < dv
+                                   ? a.S0 + (((size_t)n * H + h) * dv + v0 + t) * dk
+                                   : nullptr;
             for (int cb = 0; cb < 4; ++cb) {
                 float x[32];
 #pragma unroll
-                for (int j = 0; j < 32; ++j) x[j] = src && cb * 32 + j < dk ? src[cb * 32 + j] : 0.f;
+                for (int j = 0; j < 32; ++j)
+                    x[j] = src && cb * 32 + j < dk ? src[cb * 32 + j]
+                                                   : (is_m && cb * 32 + j == t && t < dk ? 1.f : 0.f);
                 tmem_st32(lane_addr(tbase, quad, kColS + cb * 32), x);
             }
             tmem_st_wait();
@@ -623,7 +628,8 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks) {
                 mma_f16kind(tbase + kColSW, dk + ks * (2048 >> 4), dtpp + ks * (32 >> 4), id_w, ks > 0);
-                mma_f16kind(tbase + kColU, dv + ks * (2048 >> 4), dtp + ks * (32 >> 4), id_w, ks > 0);
+                if (!is_m)  // identity rows of a propagator carry no values: U = 0
+                    mma_f16kind(tbase + kColU, dv + ks * (2048 >> 4), dtp + ks * (32 >> 4), id_w, ks > 0);
             }
             mma_commit(&s->w_mma);
         };
@@ -680,14 +686,16 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
             named_sync(1, 128);
             if (t == 32) {  // S Q^T (for the outputs) from a second thread while S W^T runs
                 tc_fence_after();
-                const uint32_t id_q = idesc_f16_f32(128, 64, 0, 0);
-                const uint64_t ds = sdesc_sw128(smem_u32(Sb), 16, 1024);
-                const uint64_t dq = sdesc_sw128(smem_u32(slot) + kSlotKQ + 8192, 16, 1024);
-                const uint32_t csq = tbase + kColSQ + sl * 64;
+                if (!prop) {
+                    const uint32_t id_q = idesc_f16_f32(128, 64, 0, 0);
+                    const uint64_t ds = sdesc_sw128(smem_u32(Sb), 16, 1024);
+                    const uint64_t dq = sdesc_sw128(smem_u32(slot) + kSlotKQ + 8192, 16, 1024);
+                    const uint32_t csq = tbase + kColSQ + sl * 64;
 #pragma unroll
-                for (int ks = 0; ks < 8; ++ks) {
-                    const uint32_t o = ((ks >> 2) * 16384 + (ks & 3) * 32) >> 4;
-                    mma_f16kind(csq, ds + o, dq + o, id_q, ks > 0);
+                    for (int ks = 0; ks < 8; ++ks) {
+                        const uint32_t o = ((ks >> 2) * 16384 + (ks & 3) * 32) >> 4;
+                        mma_f16kind(csq, ds + o, dq + o, id_q, ks > 0);
+                    }
                 }
                 mma_commit(&s->sq_done[sl]);
             }
@@ -703,7 +711,8 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
                     const uint32_t oa = ((ks >> 2) * 16384 + (ks & 3) * 32) >> 4;
-                    mma_f16kind(tbase + kColU, ds + oa, dw + ks * (2048 >> 4), id_w, 1);
+                    mma_f16kind(tbase + kColU, ds + oa, dw + ks * (2048 >> 4), id_w,
+                                !is_m || ks > 0);  // U = 0 in identity rows
                 }
                 mma_commit(&s->mma1);
             }
@@ -753,9 +762,11 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
                 for (int ks = 0; ks < 4; ++ks)
                     mma_f16kind(tbase + kColS, dvs + ks * (32 >> 4), dk + ks * (2048 >> 4), ids, 1);
                 mma_commit(&s->mma2);
+                if (!prop) {
 #pragma unroll
-                for (int ks = 0; ks < 4; ++ks)
-                    mma_f16kind(co, dvn + ks * (32 >> 4), dp + ks * (32 >> 4), ido, ks > 0);
+                    for (int ks = 0; ks < 4; ++ks)
+                        mma_f16kind(co, dvn + ks * (32 >> 4), dp + ks * (32 >> 4), ido, ks > 0);
+                }
                 mma_commit(&s->out_full[sl]);
             }
             wait_bar(&s->mma2, c & 1, false, abort_flag, a.status);
@@ -780,10 +791,12 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
         const bool aborted = __shfl_sync(0xffffffffu, *abort_flag, 0) != 0;
         if (a.S_final && !aborted) {
             // every lane takes part in the (warp-collective) TMEM loads; only
-            // rows below d_v and columns below d_k are stored
+            // rows below d_v (d_k for a propagator's identity rows) and
+            // columns below d_k are stored
             const int dk = a.dk;
-            const bool row_ok = v0 + t < dv;
-            float *dst = a.S_final + (((size_t)n * H + h) * dv + (row_ok ? v0 + t : 0)) * dk;
+            const bool row_ok = is_m ? t < dk : v0 + t < dv;
+            float *dst = is_m ? a.prop_M + (((size_t)n * H + h) * dk + (row_ok ? t : 0)) * dk
+                              : a.S_final + (((size_t)n * H + h) * dv + (row_ok ? v0 + t : 0)) * dk;
             for (int cb = 0; cb < 4 && cb * 32 < dk; ++cb) {
                 float x[32];
                 tmem_ld32(lane_addr(tbase, quad, kColS + cb * 32), x);
@@ -806,7 +819,8 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
             uint8_t *slot = sm + sl * kSlotBytes;
             const int nc = (int)min((long)kC, len - (long)c * kC);
             wait_bar(&s->tma[sl], (c >> 1) & 1, false, abort_flag, a.status);
-            convert_tiles<6>(slot + kSlotKQ, nc, t, &amax);  // K, Q (both halves), V
+            if (is_m) convert_tiles<4>(slot + kSlotKQ, nc, t, &amax);  // K, Q (both halves)
+            else convert_tiles<6>(slot + kSlotKQ, nc, t, &amax);       // and V
             fence_async_smem();
             mbar_arrive(&s->conv[sl]);
         };
@@ -830,7 +844,7 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
             const int vc = (t & 63) >> 3, ve = t & 7;
             float x[32], y[32];
 #pragma unroll 1
-            for (int half = 0; half < 2; ++half) {
+            for (int half = 0; half < (prop ? 0 : 2); ++half) {  // a propagator writes no outputs
                 tmem_ld32(lane_addr(tbase, quad, kColSQ + sl * 64 + half * 32), x);
                 tmem_ld32(lane_addr(tbase, quad, kColO + sl * 64 + half * 32), y);
                 tmem_ld_wait();
@@ -904,7 +918,9 @@ gdn_tc_kernel(const GdnArgs a, const __grid_constant__ CUtensorMap tm_q,
     const uint32_t rank = cluster_ctarank();  // 0 = producer, 1 = consumer
     const int tid = threadIdx.x, warp = tid >> 5;
     const int vt = blockIdx.x >> 1, h = blockIdx.y, n = blockIdx.z;
-    const int v0 = vt * kDVT;
+    const bool prop = a.mode == 1;
+    const bool is_m = prop && vt >= (a.dv + kDVT - 1) / kDVT;  // a propagator's identity rows
+    const int v0 = is_m ? 0 : vt * kDVT;
 
     long start = 0, len = 0;
     if (a.cu_seqlens) {
@@ -973,7 +989,7 @@ gdn_tc_kernel(const GdnArgs a, const __grid_constant__ CUtensorMap tm_q,
     const uint32_t tbase = *tmem_slot;
 
     if (rank == 0) producer(a, &tm_q, &tm_k, sm, tbase, start, len, nchunks, h);
-    else consumer(a, &tm_q, &tm_k, &tm_v, sm, tbase, start, len, nchunks, h, n, v0);
+    else consumer(a, &tm_q, &tm_k, &tm_v, sm, tbase, start, len, nchunks, h, n, v0, prop, is_m);
 
     tc_fence_before();
     __syncthreads();
@@ -1035,7 +1051,8 @@ cudaError_t gdn_launch_tc(const GdnArgs &a, cudaStream_t s, int *launches)
     cudaError_t e = cudaFuncSetAttribute(gdn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          kSmemBytes);
     if (e != cudaSuccess) return e;
-    dim3 grid(2 * ((a.dv + kDVT - 1) / kDVT), a.H, a.N);
+    // a propagator adds one 128-row tile for the d_k identity rows
+    dim3 grid(2 * ((a.dv + kDVT - 1) / kDVT + (a.mode == 1 ? 1 : 0)), a.H, a.N);
     gdn_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(a, mq, mk, mv);
     *launches = 1;
     return cudaGetLastError();

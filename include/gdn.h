@@ -131,6 +131,43 @@ gdn_status_t gdn_chunk_fwd_eta(const void *q, const void *k, const void *v,
                                void *stream);
 
 /*
+ * gdn_chunk_fwd_scan — gdn_chunk_fwd for few, long sequences: each sequence
+ * is cut into `segments` pieces at chunk boundaries that run in parallel.
+ * A segment's final state is an affine function of its initial state,
+ * S_end = S_start M + B ("从零开始的 GDN 推导", §"S 的推导": every chunk step is
+ * affine in S), and affine maps compose associatively ("Параллельность
+ * RNN?", §"Уровень 2: рекуррентность линейна, и потому ассоциативна"): a
+ * first pass computes every segment's M (d_k x d_k) and B (d_v x d_k) on the
+ * tensor cores, a scan chains them into each segment's initial state, and a
+ * second pass runs every segment's forward pass from it.  The result equals
+ * gdn_chunk_fwd up to rounding; the work is about 2 + d_k / d_v times the
+ * forward pass, spread over B * H * segments units instead of B * H.
+ *
+ * Arguments as gdn_chunk_fwd (no cu_seqlens: B sequences of T tokens), plus
+ *   segments   pieces per sequence (1..ceil(T / C)); <= 0 lets the library
+ *              choose from the device's SM count (1 means the plain pass)
+ *   workspace  device scratch of at least
+ *              gdn_chunk_fwd_scan_workspace_size(B, H, T, d_k, d_v, C,
+ *              segments) bytes, 256-byte aligned, caller-owned, not
+ *              overlapping any argument; NULL is allowed when that size is 0
+ *              or one segment is chosen.  Calls that share a workspace must
+ *              not overlap in time.
+ * Supported: bf16, C = 64, d_k <= 128 and d_k, d_v multiples of 8 (the
+ * tensor-core kernel); anything else returns GDN_ERR_UNSUPPORTED.  Four
+ * kernels are enqueued (gdn_last_launch_count reports path 3) plus one
+ * device-to-device copy per sequence for S_final.
+ */
+size_t gdn_chunk_fwd_scan_workspace_size(int B, int H, int T, int d_k, int d_v, int C,
+                                         int segments);
+
+gdn_status_t gdn_chunk_fwd_scan(const void *q, const void *k, const void *v,
+                                const float *log_alpha, const float *beta,
+                                const float *S0, void *o, float *S_final,
+                                int B, int H, int T, int d_k, int d_v, int C,
+                                gdn_dtype_t dtype, int segments,
+                                void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * gdn_decode_step — the same recurrence evaluated token by token, for decoding
  * ("从零开始的 GDN 推导", recurrent form of the gated delta rule;
  * "RNN的复兴03：现代RNN的并行计算", §一, delta-rule update), batched over
@@ -189,9 +226,10 @@ int gdn_version(void);
 
 /*
  * gdn_last_launch_count — number of kernels the last successful gdn_chunk_fwd
- * or gdn_decode_step on the calling thread enqueued, and in *path which
- * kernel family ran (0 = fp32 CUDA-core chunk kernel, 1 = tcgen05
- * tensor-core chunk kernel, 2 = recurrent decode kernel).  For
+ * gdn_chunk_fwd_scan or gdn_decode_step on the calling thread enqueued, and
+ * in *path which kernel family ran (0 = fp32 CUDA-core chunk kernel,
+ * 1 = tcgen05 tensor-core chunk kernel, 2 = recurrent decode kernel,
+ * 3 = chunk-level scan over segments).  For
  * accounting in benchmarks; no device work.
  */
 int gdn_last_launch_count(int *path);
