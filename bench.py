@@ -513,15 +513,100 @@ def run_decode(args, world, rank, local):
     print(json.dumps(line), flush=True)
 
 
+SCAN_METRIC = "GDN chunk-fwd tokens/s on one long sequence (B1 H8 T131072 d128), chunk-level scan"
+
+
+def run_scan(args, world, rank, local):
+    """The chunk-level scan on few long sequences, against the plain pass on
+    the same inputs (one unit per (sequence, head) leaves most SMs idle)."""
+    import torch
+    import gated_delta_rule_09_gb300 as gdn
+    from gated_delta_rule_09_gb300 import inputs as I
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    B, H, T, dk, dv = 1, 8, 131072, 128, 128
+    x = I.custom(B, H, T, dk, dv, 64, dtype="bf16", seed=rank)
+    keys = ("q", "k", "v", "log_alpha", "beta")
+    d = {kk: x[kk].to(dev) for kk in keys}
+    o = torch.empty(x["v"].shape, dtype=x["v"].dtype, device=dev)
+    Sf = torch.empty((B, H, dv, dk), dtype=torch.float32, device=dev)
+    need = gdn.gdn_chunk_fwd_scan_workspace_size(B, H, T, dk, dv, 64, 0)
+    ws = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(dev)
+    flops, byts = workload_numbers(I.Workload("long", B, H, T, dk, dv, 64, "bf16", True,
+                                              "sigmoid_normal", "softplus_0.1", "none"), [T] * B)
+
+    def scan_step():
+        gdn.gdn_chunk_fwd_scan(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], o=o,
+                               S_final=Sf, segments=0, workspace=ws, stream=stream)
+
+    def plain_step():
+        gdn.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], o=o, S_final=Sf,
+                          stream=stream)
+
+    def timed(fn, steps):
+        with torch.cuda.stream(stream):
+            for _ in range(max(args.warmup, 3)):
+                fn()
+        torch.cuda.synchronize(dev)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        e0.record(stream)
+        with torch.cuda.stream(stream):
+            for _ in range(steps):
+                fn()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1) / steps
+
+    plain_ms = timed(plain_step, max(1, args.steps // 10))
+    sampler = ClockSampler(local)
+    sampler.start()
+    t_start = time.time()
+    ms = timed(scan_step, args.steps)
+    t_end = time.time()
+    rows = sampler.stop()
+    assert gdn.gdn_get_device_status(stream) == 0
+    launches, path = gdn.gdn_last_launch_count()
+    ms_max = max_over_ranks(ms, world)
+    if rank != 0:
+        return
+    peaks, peak_src = load_peaks()
+    gbs = byts / (ms * 1e-3) / 1e9
+    line = {
+        "metric": SCAN_METRIC, "value": world * B * T / (ms_max * 1e-3), "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": "long_bf16: B%d H%d T%d d_k=%d d_v=%d C64, bf16, no S0" % (B, H, T, dk, dv),
+                   "segments_workspace_bytes": need, "plain_pass_ms": plain_ms,
+                   "speedup_vs_plain": plain_ms / ms,
+                   "l2": "inputs larger than L2 (%.0f MB moved per step vs %.0f MB L2)"
+                         % (byts / 1e6, L2_BYTES / 1e6),
+                   "parallelism": "replicas x%d" % world, "kernel_path": "chunk-level scan"},
+        "tflops": flops / (ms * 1e-3) / 1e12,
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": gbs / peaks["hbm_gbs"], "traffic": None, "algorithmic_bytes": byts,
+                     "peak_source": peak_src},
+        "clocks": ClockSampler.summarise(rows, t_start, t_end),
+        "gpu_launches": launches * args.steps,
+        "cpu_baseline": None,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--op", choices=["chunk", "decode"], default="chunk",
+    ap.add_argument("--op", choices=["chunk", "decode", "scan"], default="chunk",
                     help="chunk: the chunkwise forward (default); decode: the recurrent "
-                         "decode step on the decode batch")
+                         "decode step on the decode batch; scan: the chunk-level scan on "
+                         "one long sequence, beside the plain pass")
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--ref-tokens", type=int, default=256,
@@ -537,6 +622,8 @@ def main(argv=None):
         run_reference(args, world, rank)
     elif args.op == "decode":
         run_decode(args, world, rank, local)
+    elif args.op == "scan":
+        run_scan(args, world, rank, local)
     else:
         run_ours(args, world, rank, local)
     if world > 1:
