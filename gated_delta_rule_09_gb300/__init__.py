@@ -153,6 +153,38 @@ def gdn_chunk_fwd_scan(q, k, v, log_alpha, beta, S0=None, o=None, S_final=None, 
     return o, S_final
 
 
+def gdn_chunk_fwd_scan_noalloc(q, k, v, log_alpha, beta, S0=None, o=None, S_final=None, C=64,
+                               segments=0, stream=None):
+    """``gdn_chunk_fwd_scan`` on the library's fixed device scratch (no
+    workspace, nothing allocated by the call; o and S_final must then be
+    passed in to allocate nothing at all).  Calls overlapping in time race."""
+    lib = _lib.load()
+    if q.dtype not in _DTYPES:
+        raise TypeError("q/k/v dtype must be float32 or bfloat16, got %s" % q.dtype)
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _need_cuda(name, t, q.dtype)
+    _need_cuda("log_alpha", log_alpha, torch.float32)
+    _need_cuda("beta", beta, torch.float32)
+    _need_cuda("S0", S0, torch.float32)
+    if q.dim() != 4 or k.shape != q.shape or v.dim() != 4 or v.shape[:3] != q.shape[:3]:
+        raise ValueError("q, k must be [B,T,H,d_k] and v [B,T,H,d_v]")
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    if o is None:
+        o = torch.empty((B, T, H, dv), dtype=q.dtype, device=q.device)
+    if S_final is None:
+        S_final = torch.empty((B, H, dv, dk), dtype=torch.float32, device=q.device)
+    _need_cuda("o", o, q.dtype)
+    _need_cuda("S_final", S_final, torch.float32)
+    with torch.cuda.device(q.device):
+        st = lib.gdn_chunk_fwd_scan_noalloc(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(S0), _ptr(o),
+            _ptr(S_final), B, H, T, dk, dv, int(C), _DTYPES[q.dtype], int(segments),
+            ctypes.c_void_p(_stream_handle(stream, q.device)))
+    _lib.check(st)
+    return o, S_final
+
+
 def gdn_chunk_fwd_scan_workspace_size(B, H, T, d_k, d_v, C=64, segments=0):
     """Bytes of device workspace gdn_chunk_fwd_scan needs (0: none)."""
     return int(_lib.load().gdn_chunk_fwd_scan_workspace_size(B, H, T, d_k, d_v, int(C),

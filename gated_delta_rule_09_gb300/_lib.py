@@ -34,6 +34,8 @@ SIGNATURES = {
     "gdn_chunk_fwd_scan": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                                           _i, _i, _i, _i, _i, _i, _i, _i, _vp, ctypes.c_size_t,
                                           _vp]),
+    "gdn_chunk_fwd_scan_noalloc": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                                                  _i, _i, _i, _i, _i, _i, _i, _i, _vp]),
     "gdn_decode_step": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                                        _i, _i, _i, _i, _i, _i, _vp]),
     "gdn_get_device_status": (ctypes.c_int, [_vp, ctypes.POINTER(ctypes.c_uint)]),

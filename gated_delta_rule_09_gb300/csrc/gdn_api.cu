@@ -20,6 +20,15 @@ __device__ unsigned int g_status_word;
 constexpr int kMaxDevices = 64;
 unsigned int *g_status_ptr[kMaxDevices];  // per-device address of g_status_word
 
+// Fixed scratch of gdn_chunk_fwd_scan_noalloc: part of the library's device
+// image, so the call itself allocates nothing.  Every byte the scan reads is
+// written earlier in the same call (segment boundaries, start states, the
+// propagators), so nothing has to start at zero; two calls in flight at the
+// same time on one device share it and race.
+constexpr size_t kNoAllocScratchBytes = 32u << 20;
+__device__ __align__(256) unsigned char g_scan_scratch[kNoAllocScratchBytes];
+void *g_scratch_ptr[kMaxDevices];  // per-device address of g_scan_scratch
+
 gdn_status_t fail(gdn_status_t st, const char *fmt, ...)
 {
     va_list ap;
@@ -41,6 +50,23 @@ gdn_status_t status_word(unsigned int **out)
         if (e != cudaSuccess)
             return fail(GDN_ERR_CUDA, "cudaGetSymbolAddress: %s", cudaGetErrorString(e));
         __atomic_store_n(&g_status_ptr[dev], p, __ATOMIC_RELEASE);
+    }
+    *out = p;
+    return GDN_OK;
+}
+
+gdn_status_t scan_scratch(void **out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(GDN_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+    if (dev < 0 || dev >= kMaxDevices) return fail(GDN_ERR_UNSUPPORTED, "device index %d", dev);
+    void *p = __atomic_load_n(&g_scratch_ptr[dev], __ATOMIC_ACQUIRE);
+    if (!p) {
+        e = cudaGetSymbolAddress(&p, g_scan_scratch);
+        if (e != cudaSuccess)
+            return fail(GDN_ERR_CUDA, "cudaGetSymbolAddress: %s", cudaGetErrorString(e));
+        __atomic_store_n(&g_scratch_ptr[dev], p, __ATOMIC_RELEASE);
     }
     *out = p;
     return GDN_OK;
@@ -366,6 +392,29 @@ gdn_status_t gdn_chunk_fwd_scan(const void *q, const void *k, const void *v,
     t_launches = 4;
     t_path = 3;
     return GDN_OK;
+}
+
+gdn_status_t gdn_chunk_fwd_scan_noalloc(const void *q, const void *k, const void *v,
+                                        const float *log_alpha, const float *beta,
+                                        const float *S0, void *o, float *S_final,
+                                        int B, int H, int T, int d_k, int d_v, int C,
+                                        gdn_dtype_t dtype, int segments, void *stream)
+{
+    t_msg[0] = '\0';
+    const size_t need = gdn_chunk_fwd_scan_workspace_size(B, H, T, d_k, d_v, C, segments);
+    if (need > kNoAllocScratchBytes)
+        return fail(GDN_ERR_UNSUPPORTED,
+                    "this problem needs %zu bytes of scan scratch; the fixed scratch holds %zu "
+                    "(use gdn_chunk_fwd_scan with a workspace, or fewer segments)",
+                    need, kNoAllocScratchBytes);
+    void *scratch = nullptr;
+    if (need > 0) {
+        gdn_status_t st = scan_scratch(&scratch);
+        if (st != GDN_OK) return st;
+    }
+    return gdn_chunk_fwd_scan(q, k, v, log_alpha, beta, S0, o, S_final, B, H, T, d_k, d_v, C,
+                              dtype, segments, scratch, need > 0 ? kNoAllocScratchBytes : 0,
+                              stream);
 }
 
 gdn_status_t gdn_decode_step(const void *q, const void *k, const void *v,

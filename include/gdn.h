@@ -168,6 +168,27 @@ gdn_status_t gdn_chunk_fwd_scan(const void *q, const void *k, const void *v,
                                 void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * gdn_chunk_fwd_scan_noalloc — gdn_chunk_fwd_scan for callers that cannot
+ * allocate device memory: the scratch is a fixed 32 MiB array that is part of
+ * the library's device image (reserved when the library's module is loaded
+ * on a device), so the call allocates nothing.  The pages have no
+ * counterpart: this is a deployment convenience around the same scan.
+ *
+ * Arguments and results as gdn_chunk_fwd_scan without the workspace.  A
+ * problem whose scratch (gdn_chunk_fwd_scan_workspace_size with the same
+ * arguments) exceeds 32 MiB is rejected with GDN_ERR_UNSUPPORTED and a
+ * message; fewer segments need less.  Nothing in the scratch has to start
+ * at zero (each call writes every byte it reads).  The scratch is shared by
+ * every call on a device: calls that overlap in time (other streams, other
+ * threads) race and must be serialised by the caller.
+ */
+gdn_status_t gdn_chunk_fwd_scan_noalloc(const void *q, const void *k, const void *v,
+                                        const float *log_alpha, const float *beta,
+                                        const float *S0, void *o, float *S_final,
+                                        int B, int H, int T, int d_k, int d_v, int C,
+                                        gdn_dtype_t dtype, int segments, void *stream);
+
+/*
  * gdn_decode_step — the same recurrence evaluated token by token, for decoding
  * ("从零开始的 GDN 推导", recurrent form of the gated delta rule;
  * "RNN的复兴03：现代RNN的并行计算", §一, delta-rule update), batched over
