@@ -597,16 +597,102 @@ def run_scan(args, world, rank, local):
     print(json.dumps(line), flush=True)
 
 
+INV_METRIC = "UT inverse (I + A)^{-1}, 64 x 64 matrices/s, doubling product on the tensor cores"
+
+
+def run_inverse(args, world, rank, local):
+    """The batched UT inverse by both methods on the same matrices: the
+    doubling product on the tensor cores (the line's value) and the blocked
+    forward substitution on CUDA cores, with their errors against fp64."""
+    import numpy as np
+    import torch
+    import gated_delta_rule_09_gb300 as gdn
+    from gated_delta_rule_09_gb300 import inputs as I
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    count, C = 16384, 64
+    A = I.ut_matrices(count, C, 0.04, seed=rank)
+    Ad = A.to(dev)
+    T = torch.empty_like(Ad)
+    stream = torch.cuda.Stream(dev)
+
+    def timed(method, steps):
+        with torch.cuda.stream(stream):
+            for _ in range(max(args.warmup, 3)):
+                gdn.gdn_ut_inverse(Ad, T, method=method, stream=stream)
+        torch.cuda.synchronize(dev)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        e0.record(stream)
+        for _ in range(steps):
+            gdn.gdn_ut_inverse(Ad, T, method=method, stream=stream)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1) / steps
+
+    def error(method):
+        from oracle.chunk_reference import forward_substitution
+        gdn.gdn_ut_inverse(Ad, T, method=method, stream=stream)
+        torch.cuda.synchronize(dev)
+        Tc = T[:64].double().cpu().numpy()
+        An = A[:64].double().numpy()
+        worst = 0.0
+        for n in range(64):
+            ref = forward_substitution(-An[n])
+            worst = max(worst, float(np.abs(Tc[n] - ref).max() / np.abs(ref).max()))
+        return worst
+
+    fs_ms = timed(0, args.steps)
+    sampler = ClockSampler(local)
+    sampler.start()
+    t_start = time.time()
+    tc_ms = timed(1, args.steps)
+    t_end = time.time()
+    rows = sampler.stop()
+    assert gdn.gdn_get_device_status(stream) == 0
+    ms_max = max_over_ranks(tc_ms, world)
+    if rank != 0:
+        return
+    peaks, peak_src = load_peaks()
+    byts = 2 * count * C * C * 4
+    flops = count * 9 * 2 * C ** 3  # nine 64 x 64 x 64 products
+    line = {
+        "metric": INV_METRIC, "value": world * count / (ms_max * 1e-3), "unit": "matrices/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16xf16->f32",
+        "data": "synthetic",
+        "config": {"workload": "ut_inverse: %d strictly lower 64 x 64 fp32 matrices, entries "
+                               "N(0, 0.04^2)" % count,
+                   "forward_substitution_ms": fs_ms,
+                   "forward_substitution_matrices_per_s": count / (fs_ms * 1e-3),
+                   "max_rel_error_tensor": error(1), "max_rel_error_forward_substitution": error(0),
+                   "l2": "inputs larger than L2 (%.0f MB read and written per call)" % (byts / 1e6),
+                   "parallelism": "replicas x%d" % world},
+        "roofline": {"bound": "hbm", "achieved": byts / (tc_ms * 1e-3) / 1e9,
+                     "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": byts / (tc_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], "traffic": None,
+                     "algorithmic_bytes": byts, "peak_source": peak_src,
+                     "tensor_tflops": flops / (tc_ms * 1e-3) / 1e12},
+        "clocks": ClockSampler.summarise(rows, t_start, t_end),
+        "gpu_launches": args.steps,
+        "cpu_baseline": None,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--op", choices=["chunk", "decode", "scan"], default="chunk",
+    ap.add_argument("--op", choices=["chunk", "decode", "scan", "inverse"], default="chunk",
                     help="chunk: the chunkwise forward (default); decode: the recurrent "
                          "decode step on the decode batch; scan: the chunk-level scan on "
-                         "one long sequence, beside the plain pass")
+                         "one long sequence, beside the plain pass; inverse: the batched UT "
+                         "inverse by both methods")
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--ref-tokens", type=int, default=256,
@@ -624,6 +710,8 @@ def main(argv=None):
         run_decode(args, world, rank, local)
     elif args.op == "scan":
         run_scan(args, world, rank, local)
+    elif args.op == "inverse":
+        run_inverse(args, world, rank, local)
     else:
         run_ours(args, world, rank, local)
     if world > 1:

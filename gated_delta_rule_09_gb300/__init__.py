@@ -244,6 +244,24 @@ def gdn_decode_step(q, k, v, log_alpha, beta, S_in=None, o=None, S_out=None, str
     return (o.squeeze(1) if single else o), S_out
 
 
+def gdn_ut_inverse(A, T=None, method=0, stream=None):
+    """Batched T = (I + StrictLower(A))^{-1} for A [count, C, C] fp32 CUDA;
+    method 0 forward substitution (CUDA cores), 1 doubling product (tensor
+    cores).  Returns T."""
+    lib = _lib.load()
+    _need_cuda("A", A, torch.float32)
+    if A.dim() != 3 or A.shape[1] != A.shape[2]:
+        raise ValueError("A must be [count, C, C]")
+    if T is None:
+        T = torch.empty_like(A)
+    _need_cuda("T", T, torch.float32)
+    with torch.cuda.device(A.device):
+        st = lib.gdn_ut_inverse(_ptr(A), _ptr(T), A.shape[0], A.shape[1], int(method),
+                                ctypes.c_void_p(_stream_handle(stream, A.device)))
+    _lib.check(st)
+    return T
+
+
 def gdn_get_device_status(stream=None):
     """Synchronise and return (then clear) the device status bits."""
     handle = (torch.cuda.current_stream().cuda_stream if stream is None

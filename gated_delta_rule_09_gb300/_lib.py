@@ -36,6 +36,7 @@ SIGNATURES = {
                                           _vp]),
     "gdn_chunk_fwd_scan_noalloc": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                                                   _i, _i, _i, _i, _i, _i, _i, _i, _vp]),
+    "gdn_ut_inverse": (ctypes.c_int, [_vp, _vp, _i, _i, _i, _vp]),
     "gdn_decode_step": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                                        _i, _i, _i, _i, _i, _i, _vp]),
     "gdn_get_device_status": (ctypes.c_int, [_vp, ctypes.POINTER(ctypes.c_uint)]),

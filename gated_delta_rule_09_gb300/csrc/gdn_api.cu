@@ -417,6 +417,34 @@ gdn_status_t gdn_chunk_fwd_scan_noalloc(const void *q, const void *k, const void
                               stream);
 }
 
+gdn_status_t gdn_ut_inverse(const float *A, float *T, int count, int C, int method, void *stream)
+{
+    t_msg[0] = '\0';
+    if (count < 0) return fail(GDN_ERR_INVALID_ARG, "negative count %d", count);
+    if (C != 16 && C != 32 && C != 64)
+        return fail(GDN_ERR_UNSUPPORTED, "C=%d (supported: 16, 32, 64)", C);
+    if (method != 0 && method != 1)
+        return fail(GDN_ERR_UNSUPPORTED, "method %d (0: forward substitution, 1: tensor cores)",
+                    method);
+    const size_t bytes = (size_t)count * C * C * sizeof(float);
+    if (count > 0 && (!A || !T)) return fail(GDN_ERR_INVALID_ARG, "A and T must be non-NULL");
+    if (!aligned(A, 4) || !aligned(T, 4))
+        return fail(GDN_ERR_INVALID_ARG, "A and T must be 4-byte aligned");
+    if (overlaps(A, bytes, T, bytes)) return fail(GDN_ERR_INVALID_ARG, "T overlaps A");
+    t_launches = 0;
+    t_path = -1;
+    if (count == 0) return GDN_OK;
+    unsigned int *status = nullptr;
+    gdn_status_t st = status_word(&status);
+    if (st != GDN_OK) return st;
+    cudaError_t e = gdn_launch_ut_inverse(A, T, count, C, method, status,
+                                          static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail(GDN_ERR_CUDA, "UT inverse launch: %s", cudaGetErrorString(e));
+    t_launches = 1;
+    t_path = 4 + method;
+    return GDN_OK;
+}
+
 gdn_status_t gdn_decode_step(const void *q, const void *k, const void *v,
                              const float *log_alpha, const float *beta,
                              const float *S_in, void *o, float *S_out,

@@ -51,3 +51,8 @@ cudaError_t gdn_launch_scan(const float *S0, const float *Bseg, const float *Mse
                             int B, int P, int H, int dv, int dk, cudaStream_t s);
 // Segment boundaries of B equal-length sequences: cu[b * P + j] = b * T + min(j * seg, T).
 cudaError_t gdn_launch_segments(int32_t *cu, int B, int P, int T, int seg_tokens, cudaStream_t s);
+
+// Batched UT inverse T = (I + StrictLower(A))^{-1}, C <= 64: method 0 blocked
+// forward substitution (CUDA cores, fp32), 1 doubling product (tcgen05).
+cudaError_t gdn_launch_ut_inverse(const float *A, float *T, int count, int C, int method,
+                                  unsigned int *status, cudaStream_t s);

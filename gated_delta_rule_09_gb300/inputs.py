@@ -171,3 +171,14 @@ def decode_inputs(seed=0, N=256, H=16, T=1, dk=128, dv=128, dtype="bf16"):
     from a state S_in ~ N(0, sd 0.02) (returned as ``S0``); the other tensors
     as ``custom`` draws them, laid out [N, T, H, *]."""
     return custom(N, H, T, dk, dv, 64, dtype=dtype, seed=seed, s0="normal_0.02")
+
+
+def ut_matrices(count, C=64, scale=0.04, seed=0):
+    """``count`` strictly lower C x C fp32 matrices with entries ~ N(0, scale^2)
+    below the diagonal and zeros elsewhere (the UT-transform inverse's input;
+    0.04 is the spread of beta_i e^{g_i - g_j} k_i.k_j for unit keys in 128
+    dimensions, beta ~ 0.5 and in-chunk decay ~ 0.9)."""
+    rng = np.random.default_rng(seed)
+    a = rng.normal(0.0, scale, (count, C, C))
+    a *= np.tril(np.ones((C, C)), -1)
+    return torch.from_numpy(a).to(torch.float32)

@@ -232,6 +232,25 @@ gdn_status_t gdn_decode_step(const void *q, const void *k, const void *v,
                              gdn_dtype_t dtype, void *stream);
 
 /*
+ * gdn_ut_inverse — batched UT transform inverse T = (I + A)^{-1} of the
+ * chunk form ("从零开始的 GDN 推导", §"UT transform") for strictly lower C x C
+ * matrices A, by one of two methods, for comparing them:
+ *   method 0  blocked forward substitution on CUDA cores in fp32 (the
+ *             routine the tensor-core chunk kernel runs per chunk;
+ *             "RNN的复兴03：现代RNN的并行计算", §2.3.1);
+ *   method 1  the nilpotent doubling product on the tensor cores:
+ *             (I + A)^{-1} = (I - A)(I + A^2)(I + A^4)...(I + A^32) (the
+ *             finite Neumann series of the same page, §2.3.2), powers in
+ *             fp16 operands, products accumulated in fp32.
+ * A  [count, C, C] fp32 row-major; entries on and above the diagonal are
+ *    ignored.  T [count, C, C] fp32: unit diagonal, zeros above; must not
+ *    overlap A.  C in {16, 32, 64}.  One kernel; gdn_last_launch_count
+ *    reports path 4 + method.  A timed-out wait of method 1 raises
+ *    GDN_DEV_WAIT_TIMEOUT.
+ */
+gdn_status_t gdn_ut_inverse(const float *A, float *T, int count, int C, int method, void *stream);
+
+/*
  * gdn_get_device_status — synchronise `stream`, then read and clear the
  * device-side status bits (GDN_DEV_*) raised by kernels of this library on the
  * current device since the last read.  *flags receives the bits (0 = clean).
@@ -250,7 +269,8 @@ int gdn_version(void);
  * gdn_chunk_fwd_scan or gdn_decode_step on the calling thread enqueued, and
  * in *path which kernel family ran (0 = fp32 CUDA-core chunk kernel,
  * 1 = tcgen05 tensor-core chunk kernel, 2 = recurrent decode kernel,
- * 3 = chunk-level scan over segments).  For
+ * 3 = chunk-level scan over segments, 4 / 5 = UT inverse by forward
+ * substitution / on the tensor cores).  For
  * accounting in benchmarks; no device work.
  */
 int gdn_last_launch_count(int *path);

@@ -100,3 +100,21 @@ def gdn_chunk_reference_f64(q, k, v, log_alpha, beta, S0=None, C=64,
                 S = r["S_next"]
             S_final[n, h] = S
     return o, S_final
+
+
+def ut_inverse_doubling(A):
+    """(I + A)^{-1} for a strictly lower n x n A as the finite Neumann series of
+    "RNN的复兴03：现代RNN的并行计算" (§2.3.2: A is nilpotent, A^n = 0), grouped as
+    the doubling product (I - A)(I + A^2)(I + A^4)...: with X_0 = -A and
+    X_k = X_{k-1}^2, the product of (I + X_k) over X_k != 0 holds every power
+    (-A)^m, m < n, exactly once (binary expansion of m)."""
+    A = np.asarray(A, np.float64)
+    n = A.shape[0]
+    X = -A
+    T = np.eye(n) + X
+    span = 2
+    while span < n:
+        X = X @ X
+        T = T @ (np.eye(n) + X)
+        span *= 2
+    return T
