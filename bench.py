@@ -75,6 +75,17 @@ KERNEL_SOURCES = {"train_bf16": ("gdn_tc.cu", "sm100_ptx.cuh"),
                   "decode_bf16": ("gdn_decode.cu",)}
 
 
+def triangular_flops(w, lengths):
+    """The canonical count with each C x C operand counted as its lower
+    triangle (n (n + 1) / 2 entries instead of n^2)."""
+    flops = 0
+    for L in lengths:
+        full, tail = divmod(L, w.C)
+        for n in [w.C] * full + ([tail] if tail else []):
+            flops += 2 * (3 * n * w.dk * w.dv + (n * (n + 1) // 2) * (3 * w.dk + 2 * w.dv)) * w.H
+    return flops
+
+
 def kernel_source_sha(workload="train_bf16"):
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "gated_delta_rule_09_gb300", "csrc")
@@ -365,6 +376,9 @@ def run_ours(args, world, rank, local):
                    "kernel_path": "tcgen05" if path == 1 else "fp32 cuda-core"},
         "tflops": tflops,
         "pct_bf16_peak": 100.0 * tflops / peaks["bf16_tflops"],
+        "pct_bf16_sustained_peak": 100.0 * tflops / peaks.get("bf16_tflops_sustained",
+                                                                peaks["bf16_tflops"]),
+        "tflops_triangular": triangular_flops(w, lengths) / (ms * 1e-3) / 1e12,
         "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": gbs / peaks["hbm_gbs"], "traffic": recorded_traffic(w.name),
                      "algorithmic_bytes": byts, "peak_source": peak_src,
