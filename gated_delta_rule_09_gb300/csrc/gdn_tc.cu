@@ -526,11 +526,11 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
             }
             tmem_st_wait();
         }
-        // state-independent products of chunk c, issued one chunk ahead so
-        // warps 4-7 read W^T out while the state chain runs: W^T = K^T T''^T
-        // into the S W^T columns, U^T = V^T T'^T.  Needs chunk c's slot
+        // state-independent products of chunk c: W^T = K^T T''^T (for chunk 0
+        // here; later chunks' from warp 4 as soon as their tiles are ready) and
+        // U^T = V^T T'^T, issued one chunk ahead.  Needs chunk c's slot
         // (producer data and converted tiles).
-        auto issue_wu = [&](int c) {
+        auto issue_wu = [&](int c, bool with_w) {
             uint8_t *slot = sm + (c & 1) * kSlotBytes;
             const uint32_t id_w = idesc_f16_f32(128, 64, 1, 0);
             const uint32_t sa = smem_u32(slot);
@@ -540,18 +540,19 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
             const uint64_t dtp = sdesc_sw128(sa + kOutTp, 16, 1024);
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks) {
-                mma_f16kind(tbase + kColSW, dk + ks * (2048 >> 4), dtpp + ks * (32 >> 4), id_w, ks > 0);
+                if (with_w)
+                    mma_f16kind(tbase + kColSW, dk + ks * (2048 >> 4), dtpp + ks * (32 >> 4), id_w, ks > 0);
                 if (!is_m)  // identity rows of a propagator carry no values: U = 0
                     mma_f16kind(tbase + kColU, dv + ks * (2048 >> 4), dtp + ks * (32 >> 4), id_w, ks > 0);
             }
-            mma_commit(&s->w_mma);
+            if (with_w) mma_commit(&s->w_mma);
         };
         if (nchunks > 0) {
             wait_bar(&s->full[0], 0, true, abort_flag, a.status);
             wait_bar(&s->conv[0], 0, false, abort_flag, a.status);
             if (t == 0) {
                 tc_fence_after();
-                issue_wu(0);
+                issue_wu(0, true);
             }
         }
         for (int c = 0; c < nchunks; ++c) {
@@ -684,10 +685,11 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
             }
             wait_bar(&s->mma2, c & 1, false, abort_flag, a.status);
             tc_fence_after();
-            // our q/k/v tiles are consumed once S Q^T (output warps) is done too:
-            // refill them (the shipped part of the slot is handed back by warps
-            // 8-11 once the outputs are out)
-            if (t == 0 && c + 2 < nchunks && !*abort_flag) {
+            // our q/k/v tiles are consumed once S Q^T is done too: thread 64
+            // refills them while thread 0 issues the next chunk's W^T, U^T (the
+            // shipped part of the slot is handed back by warps 8-11 once the
+            // outputs are out)
+            if (t == 64 && c + 2 < nchunks && !*abort_flag) {  // beside thread 0's W^T, U^T
                 wait_bar(&s->sq_done[sl], kk & 1, false, abort_flag, a.status);
                 issue_qkv(c + 2);
             }
@@ -696,7 +698,7 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
                 wait_bar(&s->conv[sl ^ 1], ((c + 1) >> 1) & 1, false, abort_flag, a.status);
                 if (t == 0) {
                     tc_fence_after();
-                    issue_wu(c + 1);
+                    issue_wu(c + 1, false);  // W^T comes from warp 4
                 }
             }
         }
@@ -812,6 +814,26 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
         if (conv_group) {
             for (int c = 0; c < nchunks; ++c) {
                 convert(c);
+                if (c > 0) {
+                    // W^T of chunk c from here, as soon as its tiles are converted
+                    // and shipped; the W^T tile is rewritten once the chain's
+                    // first MMA batch of chunk c - 1 has read it
+                    if (t == 0) {
+                        wait_bar(&s->conv[c & 1], (c >> 1) & 1, false, abort_flag, a.status);
+                        wait_bar(&s->full[c & 1], (c >> 1) & 1, true, abort_flag, a.status);
+                        tc_fence_after();
+                        const uint32_t id_w = idesc_f16_f32(128, 64, 1, 0);
+                        const uint32_t sa = smem_u32(sm + (c & 1) * kSlotBytes);
+                        const uint64_t dk = sdesc_sw128(sa + kSlotKQ, 16384, 1024);
+                        const uint64_t dtpp = sdesc_sw128(sa + kOutTpp, 16, 1024);
+#pragma unroll
+                        for (int ks = 0; ks < 4; ++ks)
+                            mma_f16kind(tbase + kColSW, dk + ks * (2048 >> 4), dtpp + ks * (32 >> 4),
+                                        id_w, ks > 0);
+                        mma_commit(&s->w_mma);
+                    }
+                    wait_bar(&s->mma1, (c - 1) & 1, false, abort_flag, a.status);
+                }
                 w_epilogue(c);
             }
         } else {
