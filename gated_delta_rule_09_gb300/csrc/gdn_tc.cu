@@ -115,7 +115,7 @@ struct PSmall {
 struct CSmall {
     float egc[2][kC];
     uint64_t full[2], tma[2], conv[2], egc_full[2], w_mma, w_ready, mma1, mma2, out_full[2],
-        out_done[2], sq_done[2];
+        out_done[2], sq_done[2], epi1_done;
     uint32_t tmem;
     int abort_flag;
 };
@@ -526,11 +526,11 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
             }
             tmem_st_wait();
         }
-        // state-independent products of chunk c: W^T = K^T T''^T (for chunk 0
-        // here; later chunks' from warp 4 as soon as their tiles are ready) and
-        // U^T = V^T T'^T, issued one chunk ahead.  Needs chunk c's slot
-        // (producer data and converted tiles).
-        auto issue_wu = [&](int c, bool with_w) {
+        // state-independent products of chunk 0: W^T = K^T T''^T and
+        // U^T = V^T T'^T (later chunks' are issued by warp 4 as soon as their
+        // tiles are ready).  Needs chunk c's slot (producer data and converted
+        // tiles).
+        auto issue_wu = [&](int c) {
             uint8_t *slot = sm + (c & 1) * kSlotBytes;
             const uint32_t id_w = idesc_f16_f32(128, 64, 1, 0);
             const uint32_t sa = smem_u32(slot);
@@ -540,19 +540,18 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
             const uint64_t dtp = sdesc_sw128(sa + kOutTp, 16, 1024);
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks) {
-                if (with_w)
-                    mma_f16kind(tbase + kColSW, dk + ks * (2048 >> 4), dtpp + ks * (32 >> 4), id_w, ks > 0);
+                mma_f16kind(tbase + kColSW, dk + ks * (2048 >> 4), dtpp + ks * (32 >> 4), id_w, ks > 0);
                 if (!is_m)  // identity rows of a propagator carry no values: U = 0
                     mma_f16kind(tbase + kColU, dv + ks * (2048 >> 4), dtp + ks * (32 >> 4), id_w, ks > 0);
             }
-            if (with_w) mma_commit(&s->w_mma);
+            mma_commit(&s->w_mma);
         };
         if (nchunks > 0) {
             wait_bar(&s->full[0], 0, true, abort_flag, a.status);
             wait_bar(&s->conv[0], 0, false, abort_flag, a.status);
             if (t == 0) {
                 tc_fence_after();
-                issue_wu(0, true);
+                issue_wu(0);
             }
         }
         for (int c = 0; c < nchunks; ++c) {
@@ -663,6 +662,7 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
             // S += (V_new e^{g_C-g})^T K first (the chain waits for it), then
             // O_intra^T = V_new^T P^T
             if (t == 0) {
+                mbar_arrive(&s->epi1_done);  // U^T's columns are free for the next chunk
                 tc_fence_after();
                 const uint32_t ido = idesc_f16_f32(128, 64, 0, 0);
                 const uint32_t ids = idesc_f16_f32(128, 128, 0, 1);
@@ -692,14 +692,6 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
             if (t == 64 && c + 2 < nchunks && !*abort_flag) {  // beside thread 0's W^T, U^T
                 wait_bar(&s->sq_done[sl], kk & 1, false, abort_flag, a.status);
                 issue_qkv(c + 2);
-            }
-            if (c + 1 < nchunks) {  // next chunk's W^T, U^T (their columns are free now)
-                wait_bar(&s->full[sl ^ 1], ((c + 1) >> 1) & 1, true, abort_flag, a.status);
-                wait_bar(&s->conv[sl ^ 1], ((c + 1) >> 1) & 1, false, abort_flag, a.status);
-                if (t == 0) {
-                    tc_fence_after();
-                    issue_wu(c + 1, false);  // W^T comes from warp 4
-                }
             }
         }
         // one reading of the abort flag per warp keeps the branch warp-uniform
@@ -815,12 +807,14 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
             for (int c = 0; c < nchunks; ++c) {
                 convert(c);
                 if (c > 0) {
-                    // W^T of chunk c from here, as soon as its tiles are converted
-                    // and shipped; the W^T tile is rewritten once the chain's
-                    // first MMA batch of chunk c - 1 has read it
+                    // W^T and U^T of chunk c from here, as soon as its tiles are
+                    // converted and shipped; the W^T tile is rewritten once the
+                    // chain's first MMA batch of chunk c - 1 has read it
                     if (t == 0) {
                         wait_bar(&s->conv[c & 1], (c >> 1) & 1, false, abort_flag, a.status);
                         wait_bar(&s->full[c & 1], (c >> 1) & 1, true, abort_flag, a.status);
+                        // U^T's columns hold V_new^T of chunk c - 1 until its epilogue
+                        wait_bar(&s->epi1_done, (c - 1) & 1, false, abort_flag, a.status);
                         tc_fence_after();
                         const uint32_t id_w = idesc_f16_f32(128, 64, 1, 0);
                         const uint32_t sa = smem_u32(sm + (c & 1) * kSlotBytes);
@@ -830,6 +824,14 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
                         for (int ks = 0; ks < 4; ++ks)
                             mma_f16kind(tbase + kColSW, dk + ks * (2048 >> 4), dtpp + ks * (32 >> 4),
                                         id_w, ks > 0);
+                        if (!is_m) {
+                            const uint64_t dv = sdesc_sw128(sa + kSlotV, 8192, 1024);
+                            const uint64_t dtp = sdesc_sw128(sa + kOutTp, 16, 1024);
+#pragma unroll
+                            for (int ks = 0; ks < 4; ++ks)
+                                mma_f16kind(tbase + kColU, dv + ks * (2048 >> 4), dtp + ks * (32 >> 4),
+                                            id_w, ks > 0);
+                        }
                         mma_commit(&s->w_mma);
                     }
                     wait_bar(&s->mma1, (c - 1) & 1, false, abort_flag, a.status);
@@ -903,6 +905,7 @@ gdn_tc_kernel(const GdnArgs a, const __grid_constant__ CUtensorMap tm_q,
             }
             mbar_init(&s->w_mma, 1);
             mbar_init(&s->w_ready, 128);
+            mbar_init(&s->epi1_done, 1);
             mbar_init(&s->sq_done[0], 1);
             mbar_init(&s->sq_done[1], 1);
             mbar_init(&s->mma1, 1);
