@@ -477,12 +477,15 @@ __device__ __forceinline__ void producer(const GdnArgs &a, const CUtensorMap *tm
 // ======================================================================
 // consumer: the state chain and the outputs
 // ======================================================================
+// kProp: propagator mode (a compile-time switch, so the plain pass carries
+// none of its branches).
+template <bool kProp>
 __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm_q,
                                          const CUtensorMap *tm_k, const CUtensorMap *tm_v,
                                          uint8_t *sm, uint32_t tbase, long start, long len,
-                                         int nchunks, int h, int n, int v0,
-                                         bool prop, bool is_m)
+                                         int nchunks, int h, int n, int v0, bool is_m)
 {
+    constexpr bool prop = kProp;
     CSmall *s = reinterpret_cast<CSmall *>(sm + kCOffSmall);
     volatile int *abort_flag = &s->abort_flag;
     const int tid = threadIdx.x, warp = tid >> 5;
@@ -697,21 +700,50 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
         // one reading of the abort flag per warp keeps the branch warp-uniform
         const bool aborted = __shfl_sync(0xffffffffu, *abort_flag, 0) != 0;
         if (a.S_final && !aborted) {
-            // every lane takes part in the (warp-collective) TMEM loads; only
-            // rows below d_v (d_k for a propagator's identity rows) and
-            // columns below d_k are stored
+            // Each warp writes its own 32 rows: TMEM -> a padded row-major copy
+            // in the ring slot the last chunk does not use (the one before it
+            // is done: its MMAs completed before the last chunk's second batch,
+            // and no TMA or shipment follows it) -> whole rows
+            // with 16-byte stores, one 512-byte row per warp instruction.
+            // Every lane takes part in the warp-collective TMEM loads; rows
+            // at or past d_v (d_k for a propagator's identity rows) and
+            // columns at or past d_k are not stored.
             const int dk = a.dk;
-            const bool row_ok = is_m ? t < dk : v0 + t < dv;
-            float *dst = is_m ? a.prop_M + (((size_t)n * H + h) * dk + (row_ok ? t : 0)) * dk
-                              : a.S_final + (((size_t)n * H + h) * dv + (row_ok ? v0 + t : 0)) * dk;
-            for (int cb = 0; cb < 4 && cb * 32 < dk; ++cb) {
-                float x[32];
-                tmem_ld32(lane_addr(tbase, quad, kColS + cb * 32), x);
-                tmem_ld_wait();
-                if (row_ok) {
+            const int rows = is_m ? dk : min(kDVT, dv - v0);
+            const size_t row0 = is_m ? ((size_t)n * H + h) * dk : ((size_t)n * H + h) * dv + v0;
+            float *base = is_m ? a.prop_M : a.S_final;
+            constexpr int kLdF = kDK + 4;  // padded row: 16-byte stores of a warp hit distinct banks
+            float *stage_f = reinterpret_cast<float *>(sm + (nchunks & 1) * kSlotBytes) +
+                             (size_t)quad * 32 * kLdF;
+            const int lane = t & 31;
+            if ((reinterpret_cast<uintptr_t>(base) & 15) == 0) {
+                for (int cb = 0; cb < 4 && cb * 32 < dk; ++cb) {
+                    float x[32];
+                    tmem_ld32(lane_addr(tbase, quad, kColS + cb * 32), x);
+                    tmem_ld_wait();
 #pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        if (cb * 32 + j < dk) dst[cb * 32 + j] = x[j];
+                    for (int q = 0; q < 8; ++q)
+                        *reinterpret_cast<float4 *>(stage_f + lane * kLdF + cb * 32 + 4 * q) =
+                            make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
+                }
+                __syncwarp();
+                for (int rr = 0; rr < 32 && quad * 32 + rr < rows; ++rr) {
+                    if (4 * lane < dk)
+                        *reinterpret_cast<float4 *>(base + (row0 + quad * 32 + rr) * dk + 4 * lane) =
+                            *reinterpret_cast<const float4 *>(stage_f + rr * kLdF + 4 * lane);
+                }
+            } else {
+                const int r = quad * 32 + lane;
+                float *dst = base + (row0 + (r < rows ? r : 0)) * dk;
+                for (int cb = 0; cb < 4 && cb * 32 < dk; ++cb) {
+                    float x[32];
+                    tmem_ld32(lane_addr(tbase, quad, kColS + cb * 32), x);
+                    tmem_ld_wait();
+                    if (r < rows) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            if (cb * 32 + j < dk) dst[cb * 32 + j] = x[j];
+                    }
                 }
             }
         }
@@ -845,6 +877,7 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
     if (amax > kF16Max) atomicOr(a.status, 0x4u);
 }
 
+template <bool kProp>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 gdn_tc_kernel(const GdnArgs a, const __grid_constant__ CUtensorMap tm_q,
               const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v)
@@ -855,8 +888,7 @@ gdn_tc_kernel(const GdnArgs a, const __grid_constant__ CUtensorMap tm_q,
     const uint32_t rank = cluster_ctarank();  // 0 = producer, 1 = consumer
     const int tid = threadIdx.x, warp = tid >> 5;
     const int vt = blockIdx.x >> 1, h = blockIdx.y, n = blockIdx.z;
-    const bool prop = a.mode == 1;
-    const bool is_m = prop && vt >= (a.dv + kDVT - 1) / kDVT;  // a propagator's identity rows
+    const bool is_m = kProp && vt >= (a.dv + kDVT - 1) / kDVT;  // a propagator's identity rows
     const int v0 = is_m ? 0 : vt * kDVT;
 
     long start = 0, len = 0;
@@ -927,7 +959,7 @@ gdn_tc_kernel(const GdnArgs a, const __grid_constant__ CUtensorMap tm_q,
     const uint32_t tbase = *tmem_slot;
 
     if (rank == 0) producer(a, &tm_q, &tm_k, sm, tbase, start, len, nchunks, h);
-    else consumer(a, &tm_q, &tm_k, &tm_v, sm, tbase, start, len, nchunks, h, n, v0, prop, is_m);
+    else consumer<kProp>(a, &tm_q, &tm_k, &tm_v, sm, tbase, start, len, nchunks, h, n, v0, is_m);
 
     tc_fence_before();
     __syncthreads();
@@ -986,12 +1018,14 @@ cudaError_t gdn_launch_tc(const GdnArgs &a, cudaStream_t s, int *launches)
     if (!make_map(&mq, a.q, tokens, a.H, a.dk) || !make_map(&mk, a.k, tokens, a.H, a.dk) ||
         !make_map(&mv, a.v, tokens, a.H, a.dv))
         return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(gdn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    const bool prop = a.mode == 1;
+    auto kernel = prop ? gdn_tc_kernel<true> : gdn_tc_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          kSmemBytes);
     if (e != cudaSuccess) return e;
     // a propagator adds one 128-row tile for the d_k identity rows
-    dim3 grid(2 * ((a.dv + kDVT - 1) / kDVT + (a.mode == 1 ? 1 : 0)), a.H, a.N);
-    gdn_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(a, mq, mk, mv);
+    dim3 grid(2 * ((a.dv + kDVT - 1) / kDVT + (prop ? 1 : 0)), a.H, a.N);
+    kernel<<<grid, kThreads, kSmemBytes, s>>>(a, mq, mk, mv);
     *launches = 1;
     return cudaGetLastError();
 }
