@@ -477,6 +477,25 @@ __device__ __forceinline__ void producer(const GdnArgs &a, const CUtensorMap *tm
 // ======================================================================
 // consumer: the state chain and the outputs
 // ======================================================================
+// Outputs of a partial chunk (the end of a sequence), one d_v column per
+// thread: o_i = e^{g_i} (S Q^T)_i + O_intra,i for the n tokens left.  Warp-
+// collective TMEM loads: every lane of the warp calls it.
+__device__ __noinline__ void store_partial(__nv_bfloat16 *o, uint32_t sq_addr, uint32_t oi_addr,
+                                           const float *egc, int n, long tok0, int H, int h, int dv,
+                                           size_t col)
+{
+    float x[32], y[32];
+    tmem_ld32(sq_addr, x);
+    tmem_ld32(oi_addr, y);
+    tmem_ld_wait();
+    if (col < (size_t)dv) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+            if (j < n)
+                o[((size_t)(tok0 + j) * H + h) * dv + col] = __float2bfloat16_rn(fmaf(egc[j], x[j], y[j]));
+    }
+}
+
 // kProp: propagator mode (a compile-time switch, so the plain pass carries
 // none of its branches).
 template <bool kProp>
@@ -805,14 +824,10 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
                                 o + ((size_t)(tok0 + half * 32 + j) * H + h) * dv + v0 + 8 * cc) = u;
                     }
                     named_sync(3, 128);  // the staging tile is free again
-                } else if (col < (size_t)dv) {
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const int i = half * 32 + j;
-                        if (i < nc)
-                            o[((size_t)(tok0 + i) * H + h) * dv + col] =
-                                __float2bfloat16_rn(fmaf(s->egc[sl][i], x[j], y[j]));
-                    }
+                } else {
+                    store_partial(o, lane_addr(tbase, quad, kColSQ + sl * 64 + half * 32),
+                                  lane_addr(tbase, quad, kColO + sl * 64 + half * 32),
+                                  s->egc[sl] + half * 32, nc - half * 32, tok0 + half * 32, H, h, dv, col);
                 }
             }
             tc_fence_before();
