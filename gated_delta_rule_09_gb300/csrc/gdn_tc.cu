@@ -14,7 +14,8 @@
 //                       T'' = T diag(beta e^g),   T' = T diag(eta)
 //                       (eta, the write strength, is beta unless given)
 //                       W^T = K^T T''^T,          U^T = V^T T'^T
-//   state chain:        V_new^T = U^T - S W^T   (accumulated onto U^T with -W^T)
+//   state chain:        V_new^T = U^T - S W^T   (accumulated onto U^T with -W^T;
+//                       -T'' is shipped, so the W MMA yields -W^T directly)
 //                       O^T = e^{g} (S Q^T) + V_new^T P^T
 //                       S <- e^{g_C} S + (V_new * e^{g_C - g})^T K
 //
@@ -31,10 +32,11 @@
 //  * rank 1, the consumer, keeps the state slice (128 x 128 fp32) in TMEM for
 //    the whole walk and loads its own q/k/v tiles by TMA.  Warps 0-3 run the
 //    state chain (fp16 copy of S, S W^T and S Q^T, V_new, the state update
-//    and V_new^T P^T) and issue the next chunk's W^T and U^T one chunk ahead;
-//    warps 4-7 convert the q/k/v tiles to fp16 and read W^T out of TMEM into
-//    its operand tile; warps 8-11 write the outputs (through a small staging
-//    tile, 16 bytes per store).
+//    and V_new^T P^T; three of their threads issue the MMA batches, S Q^T
+//    and the TMA loads); warps 4-7 convert the q/k/v tiles to fp16, issue
+//    each chunk's W^T and U^T as soon as its tiles and the shipped data are
+//    in, and read W^T out of TMEM into its operand tile; warps 8-11 write the
+//    outputs (through a small staging tile, 16 bytes per store).
 //
 // Every MMA has M = 128, so a result row is one TMEM lane and one epilogue
 // thread.  Operands are fp16 (11-bit significand; bf16 operands would leave
@@ -74,7 +76,7 @@ constexpr int kLdX3 = gdn_ut::kUtLdX3;  // row stride of the 32x32 merge scratch
 // ---- a ring slot: what the producer ships, then the consumer's own tiles
 constexpr int kOutP = 0;           // P rows i (K-major), fp16
 constexpr int kOutTp = 8192;       // T' = T diag(eta) rows j (K-major), fp16
-constexpr int kOutTpp = 16384;     // T'' = T diag(beta e^g) rows j (K-major), fp16
+constexpr int kOutTpp = 16384;     // -T'' = -T diag(beta e^g) rows j (K-major), fp16
 constexpr int kOutG = 24576;       // g[64], e^g[64], e^{g_C-g}[64] fp32
 constexpr int kGBytes = 3 * 64 * 4;
 constexpr int kOutBytes = 25600;   // slot room for the shipped part (distributed shared
@@ -251,6 +253,19 @@ __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, bool cl
 // ======================================================================
 // producer: the state-independent part of every chunk
 // ======================================================================
+// Rows nc..63 of the four q/k tiles of a partial chunk (the end of a
+// sequence) set to zero: the loads may have brought in the next sequence.
+// Out of line, so the producer's loop stays compact.
+__device__ __noinline__ void zero_rows(uint8_t *in, int nc, int t)
+{
+    for (int idx = t; idx < 4 * (kC - nc) * 8; idx += 128) {
+        const int tile = idx / ((kC - nc) * 8), rem = idx % ((kC - nc) * 8);
+        *reinterpret_cast<uint4 *>(in + tile * 8192 + sw128(nc + (rem >> 3), rem & 7)) =
+            make_uint4(0, 0, 0, 0);
+    }
+    fence_async_smem();
+}
+
 __device__ __forceinline__ void producer(const GdnArgs &a, const CUtensorMap *tm_q,
                                          const CUtensorMap *tm_k, uint8_t *sm, uint32_t tbase,
                                          long start, long len, int nchunks, int h)
@@ -311,14 +326,7 @@ __device__ __forceinline__ void producer(const GdnArgs &a, const CUtensorMap *tm
         // q/k tiles (bf16: K K^T and Q K^T are exact products); rows past the
         // sequence are zeroed (they may hold another sequence)
         wait_bar(&s->tma_in[p], k & 1, false, abort_flag, a.status);
-        if (nc < kC) {
-            for (int idx = t; idx < 4 * (kC - nc) * 8; idx += 128) {
-                const int tile = idx / ((kC - nc) * 8), rem = idx % ((kC - nc) * 8);
-                *reinterpret_cast<uint4 *>(in + tile * 8192 + sw128(nc + (rem >> 3), rem & 7)) =
-                    make_uint4(0, 0, 0, 0);
-            }
-            fence_async_smem();
-        }
+        if (nc < kC) zero_rows(in, nc, t);
         tc_fence_before();
         named_sync(bar_id, 128);
 
@@ -361,7 +369,7 @@ __device__ __forceinline__ void producer(const GdnArgs &a, const CUtensorMap *tm
             gout[kC + t] = egt;
             gout[2 * kC + t] = __expf(gC - gt);
             s->colf[p][t] = __expf(g31 - gt);
-            s->colb[p][t] = bt * egt;  // beta e^g
+            s->colb[p][t] = -bt * egt;  // -beta e^g: the consumer's MMA gives -W^T directly
         }
         named_sync(bar_id, 128);
         wait_bar(&s->mma[p], k & 1, false, abort_flag, a.status);
@@ -424,7 +432,7 @@ __device__ __forceinline__ void producer(const GdnArgs &a, const CUtensorMap *tm
 
         // T = (I + A)^{-1}, blocked forward substitution in place
         gdn_ut::ut_inverse_64(As, Xs, t, bar_id);
-        // T'' = T diag(beta e^g) and T' = T diag(eta), both shipped
+        // -T'' = T diag(-beta e^g) and T' = T diag(eta), both shipped
         {
             const bool first = t < kC;
             const int j = first ? t : t - kC;
@@ -548,7 +556,7 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
             }
             tmem_st_wait();
         }
-        // state-independent products of chunk 0: W^T = K^T T''^T and
+        // state-independent products of chunk 0: -W^T = K^T (-T'')^T and
         // U^T = V^T T'^T (later chunks' are issued by warp 4 as soon as their
         // tiles are ready).  Needs chunk c's slot (producer data and converted
         // tiles).
@@ -708,10 +716,9 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
             wait_bar(&s->mma2, c & 1, false, abort_flag, a.status);
             tc_fence_after();
             // our q/k/v tiles are consumed once S Q^T is done too: thread 64
-            // refills them while thread 0 issues the next chunk's W^T, U^T (the
-            // shipped part of the slot is handed back by warps 8-11 once the
-            // outputs are out)
-            if (t == 64 && c + 2 < nchunks && !*abort_flag) {  // beside thread 0's W^T, U^T
+            // refills them with chunk c + 2 (the shipped part of the slot is
+            // handed back by warps 8-11 once the outputs are out)
+            if (t == 64 && c + 2 < nchunks && !*abort_flag) {
                 wait_bar(&s->sq_done[sl], kk & 1, false, abort_flag, a.status);
                 issue_qkv(c + 2);
             }
@@ -841,9 +848,7 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
             for (int half = 0; half < 2; ++half) {
                 tmem_ld32(lane_addr(tbase, quad, kColSW + half * 32), x);
                 tmem_ld_wait();
-#pragma unroll
-                for (int j = 0; j < 32; ++j) x[j] = -x[j];  // -W^T: S (-W^T) accumulates onto U^T
-#pragma unroll
+#pragma unroll  // -W^T (from -T''): S (-W^T) accumulates onto U^T
                 for (int q = 0; q < 4; ++q) st_chunk(Wt, t, half * 4 + q, x + q * 8, &amax);
             }
             fence_async_smem();
