@@ -61,7 +61,7 @@ __device__ __forceinline__ void ut_inverse_64(float *As, float *Xs, int t, uint3
         const int pp = t >> 6, r = (t & 63) >> 2, c4 = (t & 3) * 4;
         const int R = 16 * (2 * pp + 1), Cc = 32 * pp;
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4  // partial unrolling: the compact loop stays in the instruction cache
+#pragma unroll 2  // partial unrolling: the compact loop stays in the instruction cache
         for (int m = 0; m < 16; ++m) {
             const float av = As[(R + r) * kLdA + Cc + m];
             const float4 tv = *reinterpret_cast<const float4 *>(Ts + (Cc + m) * kLdA + Cc + c4);
@@ -73,7 +73,7 @@ __device__ __forceinline__ void ut_inverse_64(float *As, float *Xs, int t, uint3
         *reinterpret_cast<float4 *>(Xs + pp * 16 * kLdX2 + r * kLdX2 + c4) = acc;
         named_sync(bar_id, 128);
         acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4  // partial unrolling: the compact loop stays in the instruction cache
+#pragma unroll 2  // partial unrolling: the compact loop stays in the instruction cache
         for (int m = 0; m < 16; ++m) {
             const float tv = Ts[(R + r) * kLdA + R + m];
             const float4 xv = *reinterpret_cast<const float4 *>(Xs + pp * 16 * kLdX2 + m * kLdX2 + c4);
@@ -90,7 +90,7 @@ __device__ __forceinline__ void ut_inverse_64(float *As, float *Xs, int t, uint3
     {
         const int r2 = (t >> 3) * 2, c4 = (t & 7) * 4;
         float4 a0c = make_float4(0.f, 0.f, 0.f, 0.f), a1c = a0c;
-#pragma unroll 4
+#pragma unroll 2
         for (int m = 0; m < 32; ++m) {
             const float a0 = As[(32 + r2) * kLdA + m], a1 = As[(33 + r2) * kLdA + m];
             const float4 tv = *reinterpret_cast<const float4 *>(Ts + m * kLdA + c4);
@@ -104,7 +104,7 @@ __device__ __forceinline__ void ut_inverse_64(float *As, float *Xs, int t, uint3
         named_sync(bar_id, 128);
         a0c = make_float4(0.f, 0.f, 0.f, 0.f);
         a1c = a0c;
-#pragma unroll 4
+#pragma unroll 2
         for (int m = 0; m < 32; ++m) {
             const float t0 = Ts[(32 + r2) * kLdA + 32 + m], t1 = Ts[(33 + r2) * kLdA + 32 + m];
             const float4 xv = *reinterpret_cast<const float4 *>(Xs + m * kLdX3 + c4);
