@@ -4,14 +4,16 @@
 // T = (I + A)^{-1} for a strictly lower 64 x 64 A ("RNN的复兴03：现代RNN的并行计算",
 // §2.3.1: the column recursion T[i,j] = -sum_{m=j}^{i-1} A[i,m] T[m,j], here
 // with the sign of "从零开始的 GDN 推导", §"UT transform"), applied to blocks:
-// (1) the four 16 x 16 diagonal blocks by forward substitution, a warp per
-//     block and a lane per column, in registers;
+// (1) the four 16 x 16 diagonal blocks by forward substitution, half a warp
+//     per block and a lane per column, in registers;
 // (2) 16 -> 32: T[1,0] = -T11 (A10 T00) for the block pairs (0,1), (2,3);
 // (3) 32 -> 64: T[32:64, 0:32] = -T2 (A21 T1).
 // In place: A and T share `As` (fp32, row stride kUtLd); every block of A is
 // dead before the same block of T is written, and A's zero upper triangle is
-// exactly the zero upper blocks the merges read, so every loop has fixed
-// bounds.  `Xs` is merge scratch of 32 x kUtLdX3 floats.  128 threads (t =
+// exactly the zero upper blocks the merges read, so the loops need no
+// triangular bounds; the second product of each merge still stops at the
+// last row a warp owns, since the lower-triangular left factor is exactly
+// zero beyond it (the sums are unchanged, bit for bit).  `Xs` is merge scratch of 32 x kUtLdX3 floats.  128 threads (t =
 // 0..127, four whole warps) synchronise on named barrier `bar_id`.
 #pragma once
 
@@ -31,10 +33,11 @@ __device__ __forceinline__ void ut_inverse_64(float *As, float *Xs, int t, uint3
     float *Ts = As;
     const int lane = t & 31, quad = t >> 5;
     constexpr int kLdA = kUtLd, kLdX2 = kUtLdX2, kLdX3 = kUtLdX3;
-    // (1) 16x16 diagonal blocks: warp `quad` owns block `quad`, lane l < 16
-    //     owns column l and substitutes forward down the rows.
-    {
-        const int b = quad, l = lane;
+    // (1) 16x16 diagonal blocks on warps 0-1: lane l of warp w owns column
+    //     l & 15 of block 2w + (l >> 4) and substitutes forward down the rows
+    //     (warps 2-3 wait at the barrier).
+    if (quad < 2) {
+        const int b = 2 * quad + (lane >> 4), l = lane & 15;
         float tv[16];
 #pragma unroll
         for (int r = 0; r < 16; ++r) tv[r] = (r == l) ? 1.f : 0.f;
@@ -47,10 +50,8 @@ __device__ __forceinline__ void ut_inverse_64(float *As, float *Xs, int t, uint3
             if (r > l) tv[r] = -acc;
         }
         __syncwarp();  // every lane has read its A block before T overwrites it
-        if (l < 16) {
 #pragma unroll
-            for (int r = 0; r < 16; ++r) Ts[(16 * b + r) * kLdA + 16 * b + l] = tv[r];
-        }
+        for (int r = 0; r < 16; ++r) Ts[(16 * b + r) * kLdA + 16 * b + l] = tv[r];
     }
     named_sync(bar_id, 128);
     // (2) 16 -> 32: T[1,0] = -T11 (A10 T00) for the block pairs (0,1), (2,3).
@@ -73,8 +74,10 @@ __device__ __forceinline__ void ut_inverse_64(float *As, float *Xs, int t, uint3
         *reinterpret_cast<float4 *>(Xs + pp * 16 * kLdX2 + r * kLdX2 + c4) = acc;
         named_sync(bar_id, 128);
         acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 2  // partial unrolling: the compact loop stays in the instruction cache
-        for (int m = 0; m < 16; ++m) {
+        // T11 is lower triangular: this warp's rows r stay below mend2
+        const int mend2 = 8 * ((quad & 1) + 1);
+#pragma unroll 2
+        for (int m = 0; m < mend2; ++m) {
             const float tv = Ts[(R + r) * kLdA + R + m];
             const float4 xv = *reinterpret_cast<const float4 *>(Xs + pp * 16 * kLdX2 + m * kLdX2 + c4);
             acc.x = fmaf(tv, xv.x, acc.x);
@@ -104,8 +107,9 @@ __device__ __forceinline__ void ut_inverse_64(float *As, float *Xs, int t, uint3
         named_sync(bar_id, 128);
         a0c = make_float4(0.f, 0.f, 0.f, 0.f);
         a1c = a0c;
+        const int mend3 = 8 * (quad + 1);  // T2 is lower: this warp's rows are below mend3
 #pragma unroll 2
-        for (int m = 0; m < 32; ++m) {
+        for (int m = 0; m < mend3; ++m) {
             const float t0 = Ts[(32 + r2) * kLdA + 32 + m], t1 = Ts[(33 + r2) * kLdA + 32 + m];
             const float4 xv = *reinterpret_cast<const float4 *>(Xs + m * kLdX3 + c4);
             a0c.x = fmaf(t0, xv.x, a0c.x); a0c.y = fmaf(t0, xv.y, a0c.y);
