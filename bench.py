@@ -71,8 +71,8 @@ def workload_numbers(w, lengths):
 
 
 # Source files whose code each recorded traffic figure was measured on.
-KERNEL_SOURCES = {"train_bf16": ("gdn_tc.cu", "sm100_ptx.cuh"),
-                  "decode_bf16": ("gdn_decode.cu",)}
+KERNEL_SOURCES = {"train_bf16": ("gdn_tc.cu", "gdn_ut.cuh", "gdn_internal.h", "sm100_ptx.cuh"),
+                  "decode_bf16": ("gdn_decode.cu", "gdn_internal.h")}
 
 
 def triangular_flops(w, lengths):
