@@ -374,6 +374,22 @@ def run_ours(args, world, rank, local):
     e1.record(s_out)
     torch.cuda.synchronize(dev)
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world)
+    # the host link alone: the same input copies, no compute and no results
+    c0 = torch.cuda.Event(enable_timing=True)
+    c1 = torch.cuda.Event(enable_timing=True)
+    c0.record(s_in)
+    for i in range(e2e_steps):
+        d = sets[i & 1]
+        with torch.cuda.stream(s_in):
+            for kk in keys:
+                d[kk].copy_(host[kk], non_blocking=True)
+            if host_S0 is not None:
+                d["S0"].copy_(host_S0, non_blocking=True)
+            if host_cu is not None:
+                d["cu"].copy_(host_cu, non_blocking=True)
+    c1.record(s_in)
+    torch.cuda.synchronize(dev)
+    h2d_only_ms = max_over_ranks(c0.elapsed_time(c1) / e2e_steps, world)
     barrier(world)
 
     if rank != 0:
@@ -411,6 +427,7 @@ def run_ours(args, world, rank, local):
         "clocks": clocks,
         "e2e": {"value": world * tokens / (e2e_ms * 1e-3), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                "h2d_only_ms_per_step": h2d_only_ms,
                 "overlap": "consecutive steps: inputs in, compute, results out on three streams"},
         "gpu_launches": launches_per_step * args.steps,
         "cpu_baseline": cb,
