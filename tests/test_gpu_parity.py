@@ -222,3 +222,22 @@ def test_eta_linear_attention_limit(gdn):
                                 S0=x["S0"], eta=eta)
     assert err(o.double().cpu().numpy(), ro, "bf16") <= TOL_BF16
     assert err(S.double().cpu().numpy(), rS, "bf16", rounded=False) <= TOL_BF16
+
+
+@pytest.mark.parametrize("dk,dv", [(128, 128), (40, 24)])
+def test_final_state_unaligned_destination(gdn, dk, dv):
+    """S_final only 4-byte aligned (a view one float into a buffer): the
+    kernel's element-wise store path writes exactly what the 16-byte row
+    path writes into an aligned buffer."""
+    x = I.custom(1, 2, 200, dk, dv, 64, dtype="bf16", seed=30 + dk, s0="normal_0.02")
+    d = _dev(x)
+    _, S_al = gdn.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], S0=d["S0"], C=64)
+    n = 2 * dv * dk
+    buf = torch.full((n + 2,), -7.0, dtype=torch.float32, device="cuda")
+    S_un = buf[1:1 + n].view(1, 2, dv, dk)
+    assert S_un.data_ptr() % 16 != 0
+    gdn.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], S0=d["S0"], S_final=S_un, C=64)
+    assert gdn.gdn_get_device_status() == 0
+    assert gdn.gdn_last_launch_count()[1] == 1
+    assert torch.equal(S_un, S_al)
+    assert buf[0].item() == -7.0 and buf[-1].item() == -7.0
