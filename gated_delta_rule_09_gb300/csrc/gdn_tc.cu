@@ -96,7 +96,7 @@ constexpr int kPOffIn = 0;
 constexpr int kPOffOut = kPOffIn + kNP * kPIn;      // outgoing P | T' | T'' pool (kNOut x 24 KB)
 constexpr int kPOffSmall = kPOffOut + kNOut * kOutG;
 // ---- consumer shared memory
-constexpr int kCOffW = 2 * kSlotBytes;             // W^T rows d (MN-major B operand), fp16
+constexpr int kCOffW = 2 * kSlotBytes;             // -W^T rows d (MN-major B operand), fp16
 constexpr int kCOffSb = kCOffW + 16384;            // S as fp16, 2 d_k halves x 128 rows
 constexpr int kCOffVnT = kCOffSb + 32768;          // V_new^T rows v (K-major), fp16
 constexpr int kCOffStage = kCOffVnT + 16384;       // outputs of 32 tokens, 2 x [32][64] bf16
@@ -793,8 +793,9 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
         // back to the producer first: O_intra, the last reader of P, has
         // completed.  A full chunk is written 32 tokens at a time through an
         // 8 KB staging tile ([32 tokens][128 d_v] bf16 as two 128-byte-swizzled
-        // boxes) and two TMA stores; a partial chunk (the end of a sequence)
-        // uses plain stores so nothing lands in the next sequence.
+        // boxes) and copied out with 16-byte stores, one 256-byte token row per
+        // 16 threads; a partial chunk (the end of a sequence) uses element
+        // stores (out of line) so nothing lands in the next sequence.
         auto output = [&](int c) {
             const int sl = c & 1;
             const int nc = (int)min((long)kC, len - (long)c * kC);
