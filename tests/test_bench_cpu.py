@@ -65,3 +65,27 @@ def test_max_over_ranks_gloo_world2():
     out = mgr.dict()
     mp.spawn(_rank_main, args=(world, _free_port(), out), nprocs=world, join=True)
     assert dict(out) == {0: 2.5, 1: 2.5}
+
+
+def test_reference_arm_json_line(capsys):
+    """`bench.py --impl reference` times the oracle on the host and prints one
+    JSON line with the contract's keys (small sample: runs in about a second)."""
+    import json
+    bench.main(["--impl", "reference", "--workload", "small_bf16", "--steps", "2",
+                "--warmup", "3", "--ref-tokens", "32"])
+    lines = [ln for ln in capsys.readouterr().out.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+                "cpu_baseline", "e2e", "gpu_launches"):
+        assert key in d, key
+    assert d["impl"] == "reference" and d["steps"] == 2 and d["warmup"] == 3
+    assert d["value"] > 0 and d["unit"] == "tokens/s" and d["higher_is_better"] is True
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
+    assert d["e2e"] == {"value": d["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}
+    assert d["config"]["workload"].startswith("small_bf16")
+    # the step time matches the reported rate: B sequences x 32 tokens per step
+    w = I.WORKLOADS["small_bf16"]
+    assert abs(d["ms_per_step"] - 1e3 * w.B * 32 / d["value"]) < 1e-6 * d["ms_per_step"] + 1e-9
