@@ -222,9 +222,17 @@ def cpu_baseline(w, x, sample_tokens, min_seconds=0.0):
         if dt >= min_seconds:
             break
     tokens = reps * w.B * sample_tokens
+    # one thread on one (sequence, head) of the same sample, for the per-core rate
+    one = [t[:1, :, :1] for t in args]
+    t1 = time.perf_counter()
+    gdn_recurrence_f64(*one, n_threads=1)
+    dt1 = time.perf_counter() - t1
     return dict(value=tokens / dt, unit="tokens/s", cores=min(cores, w.B * w.H), kind="oracle",
                 sample="%d x (%d sequences x %d heads x first %d of %d tokens) of %s, fp64, "
-                       "%.2f s" % (reps, w.B, w.H, sample_tokens, w.T, w.name, dt))
+                       "%.2f s" % (reps, w.B, w.H, sample_tokens, w.T, w.name, dt),
+                one_thread={"value": sample_tokens / dt1, "unit": "token-heads/s",
+                            "sample": "1 sequence x 1 head x %d tokens, %.3f s"
+                                      % (sample_tokens, dt1)})
 
 
 def run_reference(args, world, rank):
@@ -250,7 +258,8 @@ def run_reference(args, world, rank):
                                    "on the first %d tokens of each sequence, all heads"
                                    % (w.name, w.B, w.H, w.T, w.dk, w.dv, w.C, sample)},
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cb["cores"],
-                             "kind": "oracle", "sample": cb["sample"]},
+                             "kind": "oracle", "sample": cb["sample"],
+                             "one_thread": cb["one_thread"]},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0},
             "gpu_launches": 0}

@@ -83,6 +83,7 @@ def test_reference_arm_json_line(capsys):
     assert d["impl"] == "reference" and d["steps"] == 2 and d["warmup"] == 3
     assert d["value"] > 0 and d["unit"] == "tokens/s" and d["higher_is_better"] is True
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
+    assert d["cpu_baseline"]["one_thread"]["value"] > 0
     assert d["e2e"] == {"value": d["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}
     assert d["config"]["workload"].startswith("small_bf16")
