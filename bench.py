@@ -320,6 +320,16 @@ def run_ours(args, world, rank, local):
     ms = ev0.elapsed_time(ev1) / args.steps
     ms_max = max_over_ranks(ms, world)
     clocks = ClockSampler.summarise(rows, t_start, t_end)
+    # the same steps again, each between its own pair of events, for the median
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    for i in range(args.steps):
+        evs[i][0].record(stream)
+        step(i)
+        evs[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    per_step = sorted(e0_.elapsed_time(e1_) for e0_, e1_ in evs)
+    ms_median = max_over_ranks(per_step[len(per_step) // 2], world)
 
     # end to end through the public call: every step copies its inputs from
     # pinned host memory, runs the forward pass and copies o and S_final back
@@ -413,12 +423,18 @@ def run_ours(args, world, rank, local):
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "ms_per_step_median": ms_median,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
         "data": "synthetic",
-        "config": {"workload": "%s: B%d H%d T%d d_k=%d d_v=%d C%d, bf16 q/k/v/o, fp32 gates "
-                               "and final state, no S0" % (w.name, w.B, w.H, w.T, w.dk, w.dv, w.C),
-                   "tokens_per_step": tokens, "l2": "inputs larger than L2 (%.0f MB moved per "
-                   "step vs %.0f MB L2), two resident input copies used alternately"
+        "config": {"workload": "%s: B%d H%d T%d d_k=%d d_v=%d C%d, %s q/k/v/o, fp32 gates "
+                               "and final state, %s" % (
+                                   w.name, w.B, w.H, w.T, w.dk, w.dv, w.C, w.dtype,
+                                   "no S0" if x["S0"] is None else "fp32 S0 (%s)" % w.s0),
+                   "tokens_per_step": tokens,
+                   "l2": ("inputs larger than L2 (%.0f MB moved per step vs %.0f MB L2), two "
+                          "resident input copies used alternately" if byts > L2_BYTES else
+                          "inputs fit in L2 (%.0f MB moved per step vs %.0f MB L2; not flushed, "
+                          "so warm-cache figures), two resident copies used alternately")
                    % (byts / 1e6, L2_BYTES / 1e6),
                    "parallelism": "replicas x%d" % world,
                    "kernel_path": "tcgen05" if path == 1 else "fp32 cuda-core"},
