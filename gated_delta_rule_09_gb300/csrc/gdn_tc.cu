@@ -97,8 +97,7 @@ constexpr int kPOffOut = kPOffIn + kNP * kPIn;      // outgoing P | T' | T'' poo
 constexpr int kPOffSmall = kPOffOut + kNOut * kOutG;
 // ---- consumer shared memory
 constexpr int kCOffW = 2 * kSlotBytes;             // -W^T rows d (MN-major B operand), fp16
-constexpr int kCOffSb = kCOffW + 16384;            // S as fp16, 2 d_k halves x 128 rows
-constexpr int kCOffVnT = kCOffSb + 32768;          // V_new^T rows v (K-major), fp16
+constexpr int kCOffVnT = kCOffW + 16384;           // V_new^T rows v (K-major), fp16
 constexpr int kCOffStage = kCOffVnT + 16384;       // outputs of 32 tokens, 2 x [32][64] bf16
 constexpr int kCOffSmall = kCOffStage + 8192;
 constexpr int kCSmallBytes = 3072;
@@ -110,13 +109,13 @@ constexpr int kSmemBytes = (kCOffSmall + kCSmallBytes > kPOffSmall + kPSmallByte
 struct PSmall {
     float g[kNOut][3 * kC];   // outgoing g, e^g, e^{g_C-g} (second bulk copy), pool as the tiles
     float scan[kNP][kC], beta[kNP][kC], eta[kNP][kC], colf[kNP][kC], colb[kNP][kC];
-    uint64_t tma_in[kNP], mma[kNP], shipped[kNP], slot_empty[2];
+    uint64_t tma_in[kNP], mma[kNP], shipped[kNP], slot_empty[2], gate[kNP];
     uint32_t tmem;
     int abort_flag;
 };
 struct CSmall {
     float egc[2][kC];
-    uint64_t full[2], tma[2], conv[2], egc_full[2], w_mma, w_ready, mma1, mma2, out_full[2],
+    uint64_t full[2], tma[2], conv[2], egc_full[2], w_mma, u_mma, w_ready, mma1, mma2, out_full[2],
         out_done[2], sq_done[2], epi1_done;
     uint32_t tmem;
     int abort_flag;
@@ -125,8 +124,9 @@ static_assert(sizeof(PSmall) <= kPSmallBytes && sizeof(CSmall) <= kCSmallBytes, 
 static_assert(kPXs + 32 * kLdX3 * 4 <= kPIn, "A, T and the merge scratch fit the input buffer");
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 
-// consumer TMEM columns (512): W^T | U^T then V_new^T | S Q^T x2 | O_intra^T x2 | S
-constexpr uint32_t kColSW = 0, kColU = 64, kColSQ = 128, kColO = 256, kColS = 384;
+// consumer TMEM columns (512): W^T | U^T then V_new^T | S Q^T x2 | O_intra^T |
+// S as fp16 (the A operand of S W^T and S Q^T, d_k pairs per column) | S
+constexpr uint32_t kColSW = 0, kColU = 64, kColSQ = 128, kColO = 256, kColS16 = 320, kColS = 384;
 
 __device__ __forceinline__ uint32_t pack_f16(float a, float b)
 {
@@ -134,29 +134,38 @@ __device__ __forceinline__ uint32_t pack_f16(float a, float b)
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
-__device__ __forceinline__ float max8_abs(const float *x)
+// fp16 range check: a running packed maximum of |h| over every fp16 word an
+// epilogue or conversion writes; a value outside the fp16 range became inf.
+typedef __half2 amax_t;
+__device__ __forceinline__ amax_t amax_zero() { return __float2half2_rn(0.f); }
+__device__ __forceinline__ void amax_fold(amax_t *m, uint32_t w)
 {
-    const float a = fmaxf(fabsf(x[0]), fabsf(x[1])), b = fmaxf(fabsf(x[2]), fabsf(x[3]));
-    const float c = fmaxf(fabsf(x[4]), fabsf(x[5])), d = fmaxf(fabsf(x[6]), fabsf(x[7]));
-    return fmaxf(fmaxf(a, b), fmaxf(c, d));
+    *m = __hmax2(*m, __habs2(*reinterpret_cast<const __half2 *>(&w)));
+}
+__device__ __forceinline__ bool amax_over(amax_t m)
+{
+    return fmaxf(__low2float(m), __high2float(m)) > kF16Max;
 }
 
-// 8 values -> fp16 into 16-byte chunk c of row r of a swizzled tile; their
-// magnitude folds into *amax for the range check (one dependent op per call).
-__device__ __forceinline__ void st_chunk(uint8_t *tile, int r, int c, const float *x, float *amax)
+// 8 values -> fp16 into 16-byte chunk c of row r of a swizzled tile; the
+// packed results fold into *amax for the range check.
+__device__ __forceinline__ void st_chunk(uint8_t *tile, int r, int c, const float *x, amax_t *amax)
 {
     uint4 u;
     u.x = pack_f16(x[0], x[1]);
     u.y = pack_f16(x[2], x[3]);
     u.z = pack_f16(x[4], x[5]);
     u.w = pack_f16(x[6], x[7]);
-    *amax = fmaxf(*amax, max8_abs(x));
+    amax_fold(amax, u.x);
+    amax_fold(amax, u.y);
+    amax_fold(amax, u.z);
+    amax_fold(amax, u.w);
     *reinterpret_cast<uint4 *>(tile + sw128(r, c)) = u;
 }
 
-// bf16 -> fp16 for the 8 values of one 16-byte chunk (returned), with their
-// largest magnitude folded into *amax.
-__device__ __forceinline__ uint4 chunk_bf16_to_f16(uint4 u, float *amax)
+// bf16 -> fp16 for the 8 values of one 16-byte chunk (returned), the packed
+// results folded into *amax.
+__device__ __forceinline__ uint4 chunk_bf16_to_f16(uint4 u, amax_t *amax)
 {
     const uint32_t w[4] = {u.x, u.y, u.z, u.w};
     float f[8];
@@ -166,34 +175,40 @@ __device__ __forceinline__ uint4 chunk_bf16_to_f16(uint4 u, float *amax)
         f[2 * e] = v.x;
         f[2 * e + 1] = v.y;
     }
-    *amax = fmaxf(*amax, max8_abs(f));
-    return make_uint4(pack_f16(f[0], f[1]), pack_f16(f[2], f[3]), pack_f16(f[4], f[5]),
-                      pack_f16(f[6], f[7]));
+    const uint4 r = make_uint4(pack_f16(f[0], f[1]), pack_f16(f[2], f[3]), pack_f16(f[4], f[5]),
+                               pack_f16(f[6], f[7]));
+    amax_fold(amax, r.x);
+    amax_fold(amax, r.y);
+    amax_fold(amax, r.z);
+    amax_fold(amax, r.w);
+    return r;
 }
 
 // Convert NT 64-row x 128-byte tiles (tile i at base + i * 8192) in place,
 // four 16-byte chunks per thread at a time (loads first); rows at or past
 // `nc` are zeroed (they may belong to another sequence).
 template <int NT>
-__device__ __forceinline__ void convert_tiles(uint8_t *base, int nc, int t, float *amax)
+__device__ __forceinline__ void convert_tiles(uint8_t *base, int nc, int t, amax_t *amax)
 {
-    static_assert((NT * kC * 8) % 512 == 0, "whole rounds of 4 x 128 chunks");
-#pragma unroll 1
-    for (int i0 = t; i0 < NT * kC * 8; i0 += 512) {
-        uint4 v[4];
-        uint8_t *ptr[4];
-        bool keep[4];
+    // thread t owns 16-byte column t & 7 of rows (t >> 3) + 16 j, j = 0..3,
+    // of every tile: the swizzled offsets and the row masks are fixed
+    uint32_t off[4];
+    bool keep[4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int idx = i0 + 128 * j;
-            const int r = (idx >> 3) & (kC - 1), cc = idx & 7;
-            ptr[j] = base + (idx >> 9) * 8192 + sw128(r, cc);
-            keep[j] = r < nc;
-            v[j] = *reinterpret_cast<const uint4 *>(ptr[j]);
-        }
+    for (int j = 0; j < 4; ++j) {
+        const int r = (t >> 3) + 16 * j;
+        off[j] = sw128(r, t & 7);
+        keep[j] = r < nc;
+    }
+#pragma unroll 1
+    for (int tile = 0; tile < NT; ++tile) {
+        uint8_t *tb = base + tile * 8192;
+        uint4 v[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) v[j] = *reinterpret_cast<const uint4 *>(tb + off[j]);
 #pragma unroll
         for (int j = 0; j < 4; ++j)
-            *reinterpret_cast<uint4 *>(ptr[j]) =
+            *reinterpret_cast<uint4 *>(tb + off[j]) =
                 keep[j] ? chunk_bf16_to_f16(v[j], amax) : make_uint4(0, 0, 0, 0);
     }
 }
@@ -253,6 +268,40 @@ __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, bool cl
 // ======================================================================
 // producer: the state-independent part of every chunk
 // ======================================================================
+// The A / P rows of a chunk whose total decay could push a split factor out
+// of fp32 range (every entry exponentiated on its own), out of line: it is
+// rarely taken.  Returns the range maximum of the P words it wrote.
+__device__ __noinline__ amax_t ap_extreme(uint32_t tcol, int quad, bool is_k, int i, float base, float gi,
+                                          const float *gout, float *As, uint8_t *outP)
+{
+    amax_t amax = amax_zero();
+#pragma unroll 1
+    for (int grp = 0; grp < 8; ++grp) {
+        float y[8];
+        if (grp >= 4 && quad % 2 == 0) {  // rows 0-31: all j >= 32 are zero
+#pragma unroll
+            for (int e = 0; e < 8; ++e) y[e] = 0.f;
+        } else {
+            tmem_ld8(lane_addr(tcol, quad, grp * 8), y);
+            tmem_ld_wait();
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const int j = grp * 8 + e;
+                const bool keep = is_k ? (j < i) : (j <= i);
+                y[e] = keep ? y[e] * (base * __expf(gi - gout[j])) : 0.f;
+            }
+        }
+        if (is_k) {
+            float *dst = As + i * kLdA + grp * 8;
+            *reinterpret_cast<float4 *>(dst) = make_float4(y[0], y[1], y[2], y[3]);
+            *reinterpret_cast<float4 *>(dst + 4) = make_float4(y[4], y[5], y[6], y[7]);
+        } else {
+            st_chunk(outP, i, grp, y, &amax);
+        }
+    }
+    return amax;
+}
+
 // Rows nc..63 of the four q/k tiles of a partial chunk (the end of a
 // sequence) set to zero: the loads may have brought in the next sequence.
 // Out of line, so the producer's loop stays compact.
@@ -286,7 +335,7 @@ __device__ __forceinline__ void producer(const GdnArgs &a, const CUtensorMap *tm
     const uint32_t tcol = tbase + p * 64;            // [K;Q] K^T
     const uint32_t r_full0 = mapa_shared(sm + kCOffSmall + offsetof(CSmall, full), 1);
     const uint32_t r_slot0 = mapa_shared(sm, 1);
-    float amax = 0.f;
+    amax_t amax = amax_zero();
 
     auto issue_in = [&](int c) {
         const int z = (int)(start + (long)c * kC);
@@ -325,6 +374,10 @@ __device__ __forceinline__ void producer(const GdnArgs &a, const CUtensorMap *tm
 
         // q/k tiles (bf16: K K^T and Q K^T are exact products); rows past the
         // sequence are zeroed (they may hold another sequence)
+        // the pipelines start one after another (pipeline p once p - 1 has
+        // built its first A and P), so the first chunk is not slowed by the
+        // second and third competing with it for the SM
+        if (k == 0 && p > 0) wait_bar(&s->gate[p - 1], 0, false, abort_flag, a.status);
         wait_bar(&s->tma_in[p], k & 1, false, abort_flag, a.status);
         if (nc < kC) zero_rows(in, nc, t);
         tc_fence_before();
@@ -391,6 +444,9 @@ __device__ __forceinline__ void producer(const GdnArgs &a, const CUtensorMap *tm
             const float base = is_k ? bi : 1.f;
             const float rowf = base * (split ? __expf(gi - gr) : 1.f);
             const float *colf = s->colf[p];
+            if (!split)  // extreme in-chunk decay: every entry exponentiated on its own
+                amax = __hmax2(amax, ap_extreme(tcol, quad, is_k, i, base, gi, gout, As, out + kOutP));
+            else
 #pragma unroll 1
             for (int grp = 0; grp < 8; ++grp) {
                 float y[8];
@@ -403,20 +459,11 @@ __device__ __forceinline__ void producer(const GdnArgs &a, const CUtensorMap *tm
                     const float4 c1 = *reinterpret_cast<const float4 *>(colf + grp * 8 + 4);
                     const float cf[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
                     tmem_ld_wait();
-                    if (split) {
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            const int j = grp * 8 + e;
-                            const bool keep = is_k ? (j < i) : (j <= i);
-                            y[e] = keep ? y[e] * (rowf * cf[e]) : 0.f;
-                        }
-                    } else {  // extreme in-chunk decay: exponentiate each entry
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            const int j = grp * 8 + e;
-                            const bool keep = is_k ? (j < i) : (j <= i);
-                            y[e] = keep ? y[e] * (base * __expf(gi - gout[j])) : 0.f;
-                        }
+                    for (int e = 0; e < 8; ++e) {
+                        const int j = grp * 8 + e;
+                        const bool keep = is_k ? (j < i) : (j <= i);
+                        y[e] = keep ? y[e] * (rowf * cf[e]) : 0.f;
                     }
                 }
                 if (is_k) {
@@ -431,8 +478,10 @@ __device__ __forceinline__ void producer(const GdnArgs &a, const CUtensorMap *tm
         named_sync(bar_id, 128);
 
         // T = (I + A)^{-1}, blocked forward substitution in place
+        if (k == 0 && t == 0) mbar_arrive(&s->gate[p]);
         gdn_ut::ut_inverse_64(As, Xs, t, bar_id);
-        // -T'' = T diag(-beta e^g) and T' = T diag(eta), both shipped
+        // -T'' = T diag(-beta e^g) and T' = T diag(eta), both shipped (T's upper
+        // triangle is exactly zero, so the rows go out as they are)
         {
             const bool first = t < kC;
             const int j = first ? t : t - kC;
@@ -447,8 +496,6 @@ __device__ __forceinline__ void producer(const GdnArgs &a, const CUtensorMap *tm
                 const float4 s1 = *reinterpret_cast<const float4 *>(scale + q * 8 + 4);
                 x[0] = t0.x * s0.x; x[1] = t0.y * s0.y; x[2] = t0.z * s0.z; x[3] = t0.w * s0.w;
                 x[4] = t1.x * s1.x; x[5] = t1.y * s1.y; x[6] = t1.z * s1.z; x[7] = t1.w * s1.w;
-#pragma unroll
-                for (int e = 0; e < 8; ++e) x[e] = (q * 8 + e <= j) ? x[e] : 0.f;
                 st_chunk(dst, j, q, x, &amax);
             }
         }
@@ -479,7 +526,7 @@ __device__ __forceinline__ void producer(const GdnArgs &a, const CUtensorMap *tm
             mbar_arrive(&s->shipped[p]);
         }
     }
-    if (amax > kF16Max) atomicOr(a.status, 0x4u);
+    if (amax_over(amax)) atomicOr(a.status, 0x4u);
 }
 
 // ======================================================================
@@ -518,9 +565,9 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
     const int tid = threadIdx.x, warp = tid >> 5;
     const int quad = warp & 3;
     const int H = a.H, dv = a.dv;
-    uint8_t *Sb = sm + kCOffSb, *VnT = sm + kCOffVnT, *Wt = sm + kCOffW, *stage = sm + kCOffStage;
+    uint8_t *VnT = sm + kCOffVnT, *Wt = sm + kCOffW, *stage = sm + kCOffStage;
     const uint32_t r_slot_empty = mapa_shared(sm + kPOffSmall + offsetof(PSmall, slot_empty), 0);
-    float amax = 0.f;
+    amax_t amax = amax_zero();
 
     auto issue_qkv = [&](int c) {
         uint8_t *slot = sm + (c & 1) * kSlotBytes;
@@ -569,12 +616,15 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
             const uint64_t dv = sdesc_sw128(sa + kSlotV, 8192, 1024);
             const uint64_t dtp = sdesc_sw128(sa + kOutTp, 16, 1024);
 #pragma unroll
-            for (int ks = 0; ks < 4; ++ks) {
+            for (int ks = 0; ks < 4; ++ks)
                 mma_f16kind(tbase + kColSW, dk + ks * (2048 >> 4), dtpp + ks * (32 >> 4), id_w, ks > 0);
-                if (!is_m)  // identity rows of a propagator carry no values: U = 0
+            mma_commit(&s->w_mma);  // the W epilogue starts on W^T alone
+            if (!is_m) {  // identity rows of a propagator carry no values: U = 0
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
                     mma_f16kind(tbase + kColU, dv + ks * (2048 >> 4), dtp + ks * (32 >> 4), id_w, ks > 0);
             }
-            mma_commit(&s->w_mma);
+            mma_commit(&s->u_mma);
         };
         if (nchunks > 0) {
             wait_bar(&s->full[0], 0, true, abort_flag, a.status);
@@ -609,11 +659,18 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
                     tmem_ld32(lane_addr(tbase, quad, col), x);
                     tmem_ld32(lane_addr(tbase, quad, col + 32), y);
                     tmem_ld_wait();
-                    uint8_t *box = Sb + half * 16384;
+                    // fp16 copy: column 32 half + j of this row holds d_k elements
+                    // 64 half + 2j and 64 half + 2j + 1
+                    uint32_t pk[32];
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) st_chunk(box, t, q, x + q * 8, &amax);
+                    for (int j = 0; j < 16; ++j) {
+                        pk[j] = pack_f16(x[2 * j], x[2 * j + 1]);
+                        pk[16 + j] = pack_f16(y[2 * j], y[2 * j + 1]);
+                    }
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) st_chunk(box, t, 4 + q, y + q * 8, &amax);
+                    for (int j = 0; j < 32; ++j) amax_fold(&amax, pk[j]);
+                    tmem_st32(lane_addr(tbase, quad, kColS16 + half * 32),
+                              *reinterpret_cast<const float(*)[32]>(pk));
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
                         x[j] *= dC;
@@ -631,13 +688,12 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
                 tc_fence_after();
                 if (!prop) {
                     const uint32_t id_q = idesc_f16_f32(128, 64, 0, 0);
-                    const uint64_t ds = sdesc_sw128(smem_u32(Sb), 16, 1024);
                     const uint64_t dq = sdesc_sw128(smem_u32(slot) + kSlotKQ + 8192, 16, 1024);
                     const uint32_t csq = tbase + kColSQ + sl * 64;
 #pragma unroll
                     for (int ks = 0; ks < 8; ++ks) {
                         const uint32_t o = ((ks >> 2) * 16384 + (ks & 3) * 32) >> 4;
-                        mma_f16kind(csq, ds + o, dq + o, id_q, ks > 0);
+                        mma_f16kind_ts(csq, tbase + kColS16 + ks * 8, dq + o, id_q, ks > 0);
                     }
                 }
                 mma_commit(&s->sq_done[sl]);
@@ -649,14 +705,11 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
             if (t == 0) {
                 tc_fence_after();
                 const uint32_t id_w = idesc_f16_f32(128, 64, 0, 1);
-                const uint64_t ds = sdesc_sw128(smem_u32(Sb), 16, 1024);
                 const uint64_t dw = sdesc_sw128(smem_u32(Wt), 8192, 1024);
 #pragma unroll
-                for (int ks = 0; ks < 8; ++ks) {
-                    const uint32_t oa = ((ks >> 2) * 16384 + (ks & 3) * 32) >> 4;
-                    mma_f16kind(tbase + kColU, ds + oa, dw + ks * (2048 >> 4), id_w,
-                                !is_m || ks > 0);  // U = 0 in identity rows
-                }
+                for (int ks = 0; ks < 8; ++ks)
+                    mma_f16kind_ts(tbase + kColU, tbase + kColS16 + ks * 8, dw + ks * (2048 >> 4), id_w,
+                                   !is_m || ks > 0);  // U = 0 in identity rows
                 mma_commit(&s->mma1);
             }
             wait_bar(&s->mma1, c & 1, false, abort_flag, a.status);
@@ -701,12 +754,16 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
                 const uint64_t dp = sdesc_sw128(sa + kOutP, 16, 1024);
                 const uint64_t dvs = sdesc_sw128(sa + kSlotV, 16, 1024);
                 const uint64_t dk = sdesc_sw128(sa + kSlotKQ, 16384, 1024);
-                const uint32_t co = tbase + kColO + sl * 64;
+                const uint32_t co = tbase + kColO;
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
                     mma_f16kind(tbase + kColS, dvs + ks * (32 >> 4), dk + ks * (2048 >> 4), ids, 1);
                 mma_commit(&s->mma2);
                 if (!prop) {
+                    // one O_intra buffer: chunk c - 1's outputs have read it
+                    if (c > 0)
+                        wait_bar(&s->out_done[sl ^ 1], ((c - 1) >> 1) & 1, false, abort_flag, a.status);
+                    tc_fence_after();
 #pragma unroll
                     for (int ks = 0; ks < 4; ++ks)
                         mma_f16kind(co, dvn + ks * (32 >> 4), dp + ks * (32 >> 4), ido, ks > 0);
@@ -812,7 +869,7 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
 #pragma unroll 1
             for (int half = 0; half < (prop ? 0 : 2); ++half) {  // a propagator writes no outputs
                 tmem_ld32(lane_addr(tbase, quad, kColSQ + sl * 64 + half * 32), x);
-                tmem_ld32(lane_addr(tbase, quad, kColO + sl * 64 + half * 32), y);
+                tmem_ld32(lane_addr(tbase, quad, kColO + half * 32), y);
                 tmem_ld_wait();
                 if (nc == kC) {
 #pragma unroll
@@ -834,7 +891,7 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
                     named_sync(3, 128);  // the staging tile is free again
                 } else {
                     store_partial(o, lane_addr(tbase, quad, kColSQ + sl * 64 + half * 32),
-                                  lane_addr(tbase, quad, kColO + sl * 64 + half * 32),
+                                  lane_addr(tbase, quad, kColO + half * 32),
                                   s->egc[sl] + half * 32, nc - half * 32, tok0 + half * 32, H, h, dv, col);
                 }
             }
@@ -853,6 +910,8 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
                 for (int q = 0; q < 4; ++q) st_chunk(Wt, t, half * 4 + q, x + q * 8, &amax);
             }
             fence_async_smem();
+            // the chain's first batch accumulates onto U^T: it is complete too
+            wait_bar(&s->u_mma, c & 1, false, abort_flag, a.status);
             tc_fence_before();
             mbar_arrive(&s->w_ready);
         };
@@ -877,6 +936,7 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
                         for (int ks = 0; ks < 4; ++ks)
                             mma_f16kind(tbase + kColSW, dk + ks * (2048 >> 4), dtpp + ks * (32 >> 4),
                                         id_w, ks > 0);
+                        mma_commit(&s->w_mma);
                         if (!is_m) {
                             const uint64_t dv = sdesc_sw128(sa + kSlotV, 8192, 1024);
                             const uint64_t dtp = sdesc_sw128(sa + kOutTp, 16, 1024);
@@ -885,7 +945,7 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
                                 mma_f16kind(tbase + kColU, dv + ks * (2048 >> 4), dtp + ks * (32 >> 4),
                                             id_w, ks > 0);
                         }
-                        mma_commit(&s->w_mma);
+                        mma_commit(&s->u_mma);
                     }
                     wait_bar(&s->mma1, (c - 1) & 1, false, abort_flag, a.status);
                 }
@@ -895,7 +955,7 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
             for (int c = 0; c < nchunks; ++c) output(c);
         }
     }
-    if (amax > kF16Max) atomicOr(a.status, 0x4u);
+    if (amax_over(amax)) atomicOr(a.status, 0x4u);
 }
 
 template <bool kProp>
@@ -939,6 +999,7 @@ gdn_tc_kernel(const GdnArgs a, const __grid_constant__ CUtensorMap tm_q,
                 mbar_init(&s->shipped[i], 1);
             }
             for (int i = 0; i < 2; ++i) mbar_init(&s->slot_empty[i], 1);
+            for (int i = 0; i < kNP; ++i) mbar_init(&s->gate[i], 1);
             s->abort_flag = 0;
             fence_mbar_init();
             prefetch_tensormap(&tm_q);
@@ -957,6 +1018,7 @@ gdn_tc_kernel(const GdnArgs a, const __grid_constant__ CUtensorMap tm_q,
                 mbar_init(&s->out_done[i], 128);
             }
             mbar_init(&s->w_mma, 1);
+            mbar_init(&s->u_mma, 1);
             mbar_init(&s->w_ready, 128);
             mbar_init(&s->epi1_done, 1);
             mbar_init(&s->sq_done[0], 1);
