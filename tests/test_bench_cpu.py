@@ -90,3 +90,23 @@ def test_reference_arm_json_line(capsys):
     # the step time matches the reported rate: B sequences x 32 tokens per step
     w = I.WORKLOADS["small_bf16"]
     assert abs(d["ms_per_step"] - 1e3 * w.B * 32 / d["value"]) < 1e-6 * d["ms_per_step"] + 1e-9
+
+
+def test_kernel_source_hash_covers_every_local_include():
+    """A recorded DRAM-traffic figure stays valid only while the code it was
+    measured on is unchanged: the hash must cover the kernel file and every
+    local header it includes (recursively)."""
+    import re
+    csrc = os.path.join(os.path.dirname(bench.__file__), "gated_delta_rule_09_gb300", "csrc")
+
+    def closure(name, seen):
+        if name in seen:
+            return seen
+        seen.add(name)
+        text = open(os.path.join(csrc, name)).read()
+        for inc in re.findall(r'#include "([^"]+)"', text):
+            closure(inc, seen)
+        return seen
+
+    for workload, files in bench.KERNEL_SOURCES.items():
+        assert closure(files[0], set()) == set(files), workload
