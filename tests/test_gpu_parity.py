@@ -241,3 +241,24 @@ def test_final_state_unaligned_destination(gdn, dk, dv):
     assert gdn.gdn_last_launch_count()[1] == 1
     assert torch.equal(S_un, S_al)
     assert buf[0].item() == -7.0 and buf[-1].item() == -7.0
+
+
+@pytest.mark.parametrize("la", [-3.0, -1.5, -1.2])
+def test_strong_in_chunk_decay(gdn, la):
+    """Constant log alpha: a chunk decays by e^{63 |la|} from its first token to
+    its last.  Past e^80 (la = -3.0, -1.5) the producer exponentiates every A
+    and P entry on its own instead of splitting the factor around the middle
+    of the chunk; la = -1.2 stays just inside the split form."""
+    x = I.custom(1, 2, 300, 128, 128, 64, dtype="bf16", seed=41, s0="normal_0.02")
+    x["log_alpha"] = torch.full_like(x["log_alpha"], la)
+    run_and_check(gdn, x, 64, "bf16")
+    assert gdn.gdn_last_launch_count()[1] == 1
+
+
+def test_mixed_decay_per_token(gdn):
+    """log alpha uniform in [-4, 0] per token: chunks on both sides of the
+    split threshold in one call, ragged tail included."""
+    x = I.custom(1, 3, 450, 128, 128, 64, dtype="bf16", seed=42, s0="normal_0.02")
+    g = torch.Generator().manual_seed(42)
+    x["log_alpha"] = -4.0 * torch.rand(x["log_alpha"].shape, generator=g, dtype=torch.float32)
+    run_and_check(gdn, x, 64, "bf16")
