@@ -649,7 +649,8 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
             }
             const float gC = gs[kC - 1];
 
-            // incoming state: fp16 copy for the MMAs, TMEM <- e^{g_C} S
+            // incoming state: an fp16 copy in TMEM (the A operand of S W^T and
+            // S Q^T), and TMEM <- e^{g_C} S
             {
                 const float dC = __expf(gC);
                 #pragma unroll 1
