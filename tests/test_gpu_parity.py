@@ -262,3 +262,21 @@ def test_mixed_decay_per_token(gdn):
     g = torch.Generator().manual_seed(42)
     x["log_alpha"] = -4.0 * torch.rand(x["log_alpha"].shape, generator=g, dtype=torch.float32)
     run_and_check(gdn, x, 64, "bf16")
+
+
+def test_identical_keys_extended_beta(gdn):
+    """Every token of a head has the same unit key and beta in (0, 2): A has
+    all its sub-diagonal entries from one k.k, the most correlated input the
+    UT transform meets; the state keeps one direction of k."""
+    x = I.custom(1, 2, 300, 128, 128, 64, dtype="bf16", seed=43, s0="normal_0.02", beta="uniform_0_2")
+    x["k"] = x["k"][:, :1].expand_as(x["k"]).contiguous()
+    run_and_check(gdn, x, 64, "bf16")
+    assert gdn.gdn_last_launch_count()[1] == 1
+
+
+def test_zero_keys_pure_decay(gdn):
+    """k = 0: nothing is erased or written (A = 0, T = I, W = 0), the state
+    only decays and o_t = S_t q_t."""
+    x = I.custom(1, 2, 200, 128, 128, 64, dtype="bf16", seed=44, s0="normal_0.02")
+    x["k"] = torch.zeros_like(x["k"])
+    run_and_check(gdn, x, 64, "bf16")
