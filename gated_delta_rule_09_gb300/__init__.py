@@ -37,6 +37,47 @@ def load():
     return _lib.load()
 
 
+def _check_args(q, k, v, log_alpha, beta, eta, S0, o, S_final, packed):
+    """Types, devices and shapes of one forward call; every tensor the kernels
+    read or write is checked against the sizes the C call derives from q and v,
+    so a wrongly shaped argument is refused here instead of being read or
+    written past its end.  Returns (B, T, H, d_k, d_v, N)."""
+    if q.dtype not in _DTYPES:
+        raise TypeError("q/k/v dtype must be float32 or bfloat16, got %s" % q.dtype)
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _need_cuda(name, t, q.dtype)
+    _need_cuda("log_alpha", log_alpha, torch.float32)
+    _need_cuda("beta", beta, torch.float32)
+    _need_cuda("eta", eta, torch.float32)
+    _need_cuda("S0", S0, torch.float32)
+    _need_cuda("o", o, q.dtype)
+    _need_cuda("S_final", S_final, torch.float32)
+    if q.dim() != 4 or k.shape != q.shape or v.dim() != 4 or v.shape[:3] != q.shape[:3]:
+        raise ValueError("q, k must be [B,T,H,d_k] and v [B,T,H,d_v]")
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    if log_alpha.shape != (B, T, H) or beta.shape != (B, T, H):
+        raise ValueError("log_alpha and beta must be [B,T,H] = %s" % ((B, T, H),))
+    if eta is not None and eta.shape != (B, T, H):
+        raise ValueError("eta must be [B,T,H] = %s" % ((B, T, H),))
+    if packed is not None:
+        _need_cuda("cu_seqlens", packed, torch.int32)
+        if B != 1:
+            raise ValueError("packed (cu_seqlens) inputs must have B == 1")
+        if packed.dim() != 1 or packed.numel() < 2:
+            raise ValueError("cu_seqlens must be a 1-D int32 tensor of N + 1 >= 2 offsets")
+        N = packed.numel() - 1
+    else:
+        N = B
+    if S0 is not None and S0.shape != (N, H, dv, dk):
+        raise ValueError("S0 must be [N,H,d_v,d_k] = %s" % ((N, H, dv, dk),))
+    if o is not None and o.shape != (B, T, H, dv):
+        raise ValueError("o must be [B,T,H,d_v] = %s" % ((B, T, H, dv),))
+    if S_final is not None and S_final.shape != (N, H, dv, dk):
+        raise ValueError("S_final must be [N,H,d_v,d_k] = %s" % ((N, H, dv, dk),))
+    return B, T, H, dk, dv, N
+
+
 def gdn_chunk_fwd(q, k, v, log_alpha, beta, S0=None, o=None, S_final=None,
                   C=64, cu_seqlens=None, stream=None, want_final_state=True):
     """Chunkwise gated delta rule forward; returns ``(o, S_final)``.
@@ -64,38 +105,12 @@ def gdn_chunk_fwd_eta(q, k, v, log_alpha, beta, eta, S0=None, o=None, S_final=No
 
 def _chunk(q, k, v, log_alpha, beta, eta, S0, o, S_final, C, cu_seqlens, stream,
            want_final_state):
+    B, T, H, dk, dv, N = _check_args(q, k, v, log_alpha, beta, eta, S0, o, S_final, cu_seqlens)
     lib = _lib.load()
-    if q.dtype not in _DTYPES:
-        raise TypeError("q/k/v dtype must be float32 or bfloat16, got %s" % q.dtype)
-    for name, t in (("q", q), ("k", k), ("v", v)):
-        _need_cuda(name, t, q.dtype)
-    _need_cuda("log_alpha", log_alpha, torch.float32)
-    _need_cuda("beta", beta, torch.float32)
-    _need_cuda("eta", eta, torch.float32)
-    _need_cuda("S0", S0, torch.float32)
-    _need_cuda("cu_seqlens", cu_seqlens, torch.int32)
-    if q.dim() != 4 or k.shape != q.shape or v.dim() != 4 or v.shape[:3] != q.shape[:3]:
-        raise ValueError("q, k must be [B,T,H,d_k] and v [B,T,H,d_v]")
-    B, T, H, dk = q.shape
-    dv = v.shape[-1]
-    if log_alpha.shape != (B, T, H) or beta.shape != (B, T, H):
-        raise ValueError("log_alpha and beta must be [B,T,H]")
-    if eta is not None and eta.shape != (B, T, H):
-        raise ValueError("eta must be [B,T,H]")
-    if cu_seqlens is not None:
-        if B != 1:
-            raise ValueError("packed (cu_seqlens) inputs must have B == 1")
-        N = cu_seqlens.numel() - 1
-    else:
-        N = B
-    if S0 is not None and S0.shape != (N, H, dv, dk):
-        raise ValueError("S0 must be [N,H,d_v,d_k] = %s" % ((N, H, dv, dk),))
     if o is None:
         o = torch.empty((B, T, H, dv), dtype=q.dtype, device=q.device)
-    _need_cuda("o", o, q.dtype)
     if S_final is None and want_final_state:
         S_final = torch.empty((N, H, dv, dk), dtype=torch.float32, device=q.device)
-    _need_cuda("S_final", S_final, torch.float32)
     handle = ctypes.c_void_p(_stream_handle(stream, q.device))
     with torch.cuda.device(q.device):
         if eta is None:
@@ -118,28 +133,12 @@ def gdn_chunk_fwd_scan(q, k, v, log_alpha, beta, S0=None, o=None, S_final=None, 
     run in parallel (0 = chosen by the library); returns ``(o, S_final)``.
     ``workspace`` is a uint8 CUDA tensor of at least
     ``gdn_chunk_fwd_scan_workspace_size(...)`` bytes, allocated here if None."""
+    B, T, H, dk, dv, _ = _check_args(q, k, v, log_alpha, beta, None, S0, o, S_final, None)
     lib = _lib.load()
-    if q.dtype not in _DTYPES:
-        raise TypeError("q/k/v dtype must be float32 or bfloat16, got %s" % q.dtype)
-    for name, t in (("q", q), ("k", k), ("v", v)):
-        _need_cuda(name, t, q.dtype)
-    _need_cuda("log_alpha", log_alpha, torch.float32)
-    _need_cuda("beta", beta, torch.float32)
-    _need_cuda("S0", S0, torch.float32)
-    if q.dim() != 4 or k.shape != q.shape or v.dim() != 4 or v.shape[:3] != q.shape[:3]:
-        raise ValueError("q, k must be [B,T,H,d_k] and v [B,T,H,d_v]")
-    B, T, H, dk = q.shape
-    dv = v.shape[-1]
-    if log_alpha.shape != (B, T, H) or beta.shape != (B, T, H):
-        raise ValueError("log_alpha and beta must be [B,T,H]")
-    if S0 is not None and S0.shape != (B, H, dv, dk):
-        raise ValueError("S0 must be [B,H,d_v,d_k] = %s" % ((B, H, dv, dk),))
     if o is None:
         o = torch.empty((B, T, H, dv), dtype=q.dtype, device=q.device)
-    _need_cuda("o", o, q.dtype)
     if S_final is None:
         S_final = torch.empty((B, H, dv, dk), dtype=torch.float32, device=q.device)
-    _need_cuda("S_final", S_final, torch.float32)
     with torch.cuda.device(q.device):
         need = gdn_chunk_fwd_scan_workspace_size(B, H, T, dk, dv, C, segments)
         if workspace is None:
@@ -158,24 +157,12 @@ def gdn_chunk_fwd_scan_noalloc(q, k, v, log_alpha, beta, S0=None, o=None, S_fina
     """``gdn_chunk_fwd_scan`` on the library's fixed device scratch (no
     workspace, nothing allocated by the call; o and S_final must then be
     passed in to allocate nothing at all).  Calls overlapping in time race."""
+    B, T, H, dk, dv, _ = _check_args(q, k, v, log_alpha, beta, None, S0, o, S_final, None)
     lib = _lib.load()
-    if q.dtype not in _DTYPES:
-        raise TypeError("q/k/v dtype must be float32 or bfloat16, got %s" % q.dtype)
-    for name, t in (("q", q), ("k", k), ("v", v)):
-        _need_cuda(name, t, q.dtype)
-    _need_cuda("log_alpha", log_alpha, torch.float32)
-    _need_cuda("beta", beta, torch.float32)
-    _need_cuda("S0", S0, torch.float32)
-    if q.dim() != 4 or k.shape != q.shape or v.dim() != 4 or v.shape[:3] != q.shape[:3]:
-        raise ValueError("q, k must be [B,T,H,d_k] and v [B,T,H,d_v]")
-    B, T, H, dk = q.shape
-    dv = v.shape[-1]
     if o is None:
         o = torch.empty((B, T, H, dv), dtype=q.dtype, device=q.device)
     if S_final is None:
         S_final = torch.empty((B, H, dv, dk), dtype=torch.float32, device=q.device)
-    _need_cuda("o", o, q.dtype)
-    _need_cuda("S_final", S_final, torch.float32)
     with torch.cuda.device(q.device):
         st = lib.gdn_chunk_fwd_scan_noalloc(
             _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(S0), _ptr(o),
@@ -207,7 +194,6 @@ def gdn_decode_step(q, k, v, log_alpha, beta, S_in=None, o=None, S_out=None, str
     S_in [N,H,d_v,d_k] fp32 or None (zeros).  ``S_out`` may be ``S_in`` for an
     in-place update; if None a new tensor is allocated.
     """
-    lib = _lib.load()
     if q.dtype not in _DTYPES:
         raise TypeError("q/k/v dtype must be float32 or bfloat16, got %s" % q.dtype)
     single = q.dim() == 3
@@ -232,9 +218,14 @@ def gdn_decode_step(q, k, v, log_alpha, beta, S_in=None, o=None, S_out=None, str
     elif single:
         o = o.unsqueeze(1)
     _need_cuda("o", o, q.dtype)
+    if o.shape != (N, T, H, dv):
+        raise ValueError("o must be [N,T,H,d_v] (or [N,H,d_v] for one token)")
     if S_out is None:
         S_out = torch.empty((N, H, dv, dk), dtype=torch.float32, device=q.device)
     _need_cuda("S_out", S_out, torch.float32)
+    if S_out.shape != (N, H, dv, dk):
+        raise ValueError("S_out must be [N,H,d_v,d_k] = %s" % ((N, H, dv, dk),))
+    lib = _lib.load()
     with torch.cuda.device(q.device):
         st = lib.gdn_decode_step(
             _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(S_in),
