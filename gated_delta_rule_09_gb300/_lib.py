@@ -21,6 +21,7 @@ GDN_BF16 = 1
 GDN_DEV_BAD_SEQLENS = 0x1
 GDN_DEV_WAIT_TIMEOUT = 0x2
 GDN_DEV_F16_RANGE = 0x4
+GDN_DEV_F16_PRECISION = 0x8
 
 # (name, restype, argtypes) for every entry point of include/gdn.h
 _vp = ctypes.c_void_p

@@ -53,6 +53,8 @@ typedef enum { GDN_F32 = 0, GDN_BF16 = 1 } gdn_dtype_t;
 #define GDN_DEV_BAD_SEQLENS 0x1u /* a cu_seqlens span was negative or past T */
 #define GDN_DEV_WAIT_TIMEOUT 0x2u /* a bounded pipeline wait gave up          */
 #define GDN_DEV_F16_RANGE 0x4u    /* a tensor-core operand left the fp16 range  */
+#define GDN_DEV_F16_PRECISION 0x8u /* a unit's state-chain operands all stayed
+                                      below 2^-10: fp16 kept few bits of them   */
 
 /*
  * gdn_chunk_fwd — forward pass of the gated delta rule, chunkwise.
@@ -87,9 +89,15 @@ typedef enum { GDN_F32 = 0, GDN_BF16 = 1 } gdn_dtype_t;
  *              GDN_DEV_BAD_SEQLENS (see gdn_get_device_status).
  *   dtype      GDN_F32 or GDN_BF16 (q, k, v and o share it).  fp32 runs in
  *              fp32 on CUDA cores.  bf16 runs on the tensor cores with fp16
- *              operands (11-bit significand; bf16 inputs convert exactly for
- *              |x| < 65504) and fp32 accumulation and state; an operand that
- *              leaves the fp16 range raises GDN_DEV_F16_RANGE
+ *              operands (11-bit significand) and fp32 accumulation and
+ *              state.  A bf16 input converts to fp16 exactly when its
+ *              magnitude lies in [2^-14, 65504]; below 2^-14 fp16 keeps fewer
+ *              bits (subnormals), above 65504 it overflows.  An operand that
+ *              leaves the fp16 range raises GDN_DEV_F16_RANGE; a (sequence,
+ *              head) whose state chain ran entirely below 2^-10 in magnitude
+ *              (e.g. v and S0 of order 1e-6) raises GDN_DEV_F16_PRECISION:
+ *              the method is linear in v and S0, so scaling both up (and the
+ *              results back down) avoids it
  *   stream     cudaStream_t to enqueue on
  *
  * Alignment: q, k, v, o must be aligned to 16 bytes; log_alpha, beta, S0 and

@@ -30,6 +30,9 @@ def run_and_check(gdn, x, C, dtype, S0=None, want_S=True, tol=None):
                                 S0=x["S0"], cu_seqlens=x["cu_seqlens"])
     tol = tol or (TOL_F32 if dtype == "f32" else TOL_BF16)
     eo = err(o.double().cpu().numpy(), ro, dtype)
+    if dtype == "bf16":  # the raw figure beside the net one (the bound is on the net one)
+        print("o error: net of half a bf16 ulp %.4f, raw max|o-ref|/RMS %.4f"
+              % (eo, err(o.double().cpu().numpy(), ro, dtype, rounded=False)))
     assert np.isfinite(eo) and eo <= tol, ("o", eo)
     if want_S:
         es = err(S.double().cpu().numpy(), rS, dtype, rounded=False)
