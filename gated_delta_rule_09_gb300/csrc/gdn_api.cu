@@ -265,6 +265,8 @@ gdn_status_t gdn_get_device_status(void *stream, unsigned int *flags)
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return fail(GDN_ERR_CUDA, "reading device status: %s", cudaGetErrorString(e));
     *flags = v;
+    if (v & GDN_DEV_WAIT_TIMEOUT)
+        return fail(GDN_ERR_TIMEOUT, "a bounded device wait ran out (flags %#x): outputs invalid", v);
     return GDN_OK;
 }
 

@@ -46,7 +46,8 @@
 // fp16; K K^T and Q K^T keep bf16 operands (exact products).  Accumulation
 // and the state are fp32.  Values outside the fp16 range raise
 // GDN_DEV_F16_RANGE.  Every wait is bounded: on timeout the CTA raises
-// GDN_DEV_WAIT_TIMEOUT and stops waiting, so the kernel always finishes.
+// GDN_DEV_WAIT_TIMEOUT and winds down (later waits are bounded by 50 us,
+// enough for what is in flight to complete), so the kernel always finishes.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -68,7 +69,17 @@ constexpr int kDVT = 128;    // d_v rows per unit (rows past d_v are zero paddin
 constexpr int kThreads = 384;  // producer: 3 pipelines x 4 warps; consumer: 3 x 4 warps
 constexpr int kNP = 3;         // producer pipelines (chunk c goes to pipeline c % 3)
 constexpr int kNOut = 5;       // outgoing buffers (chunk c uses buffer c % 5)
+#ifndef GDN_WAIT_TEST
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
+constexpr bool kWaitTest = false;
+#else
+// Test build: 5 ms per wait, and the producer of the unit (sequence 0, head 0,
+// first d_v tile) withholds one software arrival (the "shipped" signal of
+// chunk 1), so a wait runs out and the abort path runs on real hardware.
+constexpr uint64_t kWaitLimitNs = 5000000ull;
+constexpr bool kWaitTest = true;
+#endif
+constexpr uint64_t kDrainNs = 50000;  // a wait's bound once the CTA has aborted
 constexpr float kF16Max = 65504.f;
 constexpr int kLdA = gdn_ut::kUtLd;     // fp32 row stride of A / T
 constexpr int kLdX3 = gdn_ut::kUtLdX3;  // row stride of the 32x32 merge scratch
@@ -219,19 +230,23 @@ __device__ __forceinline__ uint32_t lane_addr(uint32_t tbase, int quad, uint32_t
     return tbase + (static_cast<uint32_t>(quad * 32) << 16) + col;
 }
 
-// Bounded waits, kept out of line (about twenty call sites): once this CTA has
-// given up on one wait, every later wait returns immediately so the kernel
-// winds down.
+// Bounded waits, kept out of line (about twenty call sites), without calls of
+// their own.  Once this CTA has given up on one wait (GDN_DEV_WAIT_TIMEOUT),
+// every wait that starts later is bounded by kDrainNs instead, so the kernel
+// winds down in milliseconds while the completions it still awaits come in:
+// every MMA batch, TMA load and shipment in flight is awaited by the walk that
+// follows it, and those finish in microseconds, so nothing asynchronous
+// outlives the CTA's tensor memory.  An aborted CTA issues no new TMA load or
+// shipment, and an aborted consumer releases no ring slot.
 __device__ __noinline__ bool wait_cta(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
                                       unsigned int *status)
 {
-    if (*abort_flag) return false;
+    const uint64_t lim = *abort_flag ? kDrainNs : kWaitLimitNs;
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (;;) {
         if (mbar_try_wait(bar, parity)) return true;
-        if (*abort_flag) return false;
-        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        if (globaltimer_ns() - t0 > lim) {
             *abort_flag = 1;
             atomicOr(status, 0x2u);
             return false;
@@ -242,13 +257,12 @@ __device__ __noinline__ bool wait_cta(uint64_t *bar, uint32_t parity, volatile i
 __device__ __noinline__ bool wait_cluster(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
                                           unsigned int *status)
 {
-    if (*abort_flag) return false;
+    const uint64_t lim = *abort_flag ? kDrainNs : kWaitLimitNs;
     if (mbar_try_wait_cluster(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (;;) {
         if (mbar_try_wait_cluster(bar, parity)) return true;
-        if (*abort_flag) return false;
-        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        if (globaltimer_ns() - t0 > lim) {
             *abort_flag = 1;
             atomicOr(status, 0x2u);
             return false;
@@ -517,14 +531,15 @@ __device__ __forceinline__ void producer(const GdnArgs &a, const CUtensorMap *tm
                               a.status);
             ok = ok && wait_bar(&s->slot_empty[c & 1], ((c >> 1) + 1) & 1, true, abort_flag,
                                 a.status);
-            if (ok) {
+            if (ok && !*abort_flag) {
                 const uint32_t r_full = r_full0 + (c & 1) * sizeof(uint64_t);
                 const uint32_t r_slot = r_slot0 + (c & 1) * kSlotBytes;
                 mbar_arrive_expect_tx_remote(r_full, kOutG + kGBytes);
                 bulk_copy_to_peer(r_slot, out, kOutG, r_full);
                 bulk_copy_to_peer(r_slot + kOutG, gout, kGBytes, r_full);
             }
-            mbar_arrive(&s->shipped[p]);
+            if (!(kWaitTest && c == 1 && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0))
+                mbar_arrive(&s->shipped[p]);
         }
     }
     if (amax_over(amax)) atomicOr(a.status, 0x4u);
@@ -644,6 +659,7 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
             wait_bar(&s->out_done[sl], (kk + 1) & 1, false, abort_flag, a.status);
             if (c > 0)  // S Q^T of chunk c - 1 (another thread's MMAs) has read the fp16 S copy
                 wait_bar(&s->sq_done[sl ^ 1], ((c - 1) >> 1) & 1, false, abort_flag, a.status);
+            tc_fence_after();  // the S copy below overwrites what S Q^T of chunk c - 1 read
             if (t < kC) {
                 s->egc[sl][t] = gs[kC + t];
                 mbar_arrive(&s->egc_full[sl]);
@@ -877,7 +893,9 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
             wait_bar(&s->out_full[sl], (c >> 1) & 1, false, abort_flag, a.status);
             wait_bar(&s->sq_done[sl], (c >> 1) & 1, false, abort_flag, a.status);
             tc_fence_after();
-            if (t == 0) mbar_arrive_remote(r_slot_empty + sl * sizeof(uint64_t));
+            // released only while the walk is live: after an abort nothing more
+            // is shipped into the ring
+            if (t == 0 && !*abort_flag) mbar_arrive_remote(r_slot_empty + sl * sizeof(uint64_t));
             const size_t col = (size_t)v0 + t;
             uint8_t *box = stage + (t >> 6) * 4096;  // d_v half of this thread
             const int vc = (t & 63) >> 3, ve = t & 7;

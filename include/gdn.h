@@ -43,8 +43,9 @@ typedef enum {
     GDN_ERR_INVALID_ARG = 1, /* null/misaligned pointer, bad size, overlap   */
     GDN_ERR_UNSUPPORTED = 2, /* shape or dtype outside the compiled set      */
     GDN_ERR_CUDA = 3,        /* a CUDA runtime call or a launch failed        */
-    GDN_ERR_TIMEOUT = 4,     /* reserved: a bounded device wait ran out       */
-    GDN_ERR_INTERNAL = 5     /* reserved: inconsistent internal state         */
+    GDN_ERR_TIMEOUT = 4      /* gdn_get_device_status: a bounded device wait
+                                ran out (GDN_DEV_WAIT_TIMEOUT is among the
+                                flags; the results of that call are invalid) */
 } gdn_status_t;
 
 typedef enum { GDN_F32 = 0, GDN_BF16 = 1 } gdn_dtype_t;
@@ -262,6 +263,10 @@ gdn_status_t gdn_ut_inverse(const float *A, float *T, int count, int C, int meth
  * gdn_get_device_status — synchronise `stream`, then read and clear the
  * device-side status bits (GDN_DEV_*) raised by kernels of this library on the
  * current device since the last read.  *flags receives the bits (0 = clean).
+ * Returns GDN_ERR_TIMEOUT when GDN_DEV_WAIT_TIMEOUT is among them (*flags is
+ * still written): a kernel gave up on a bounded wait, finished without
+ * completing its work, drained what it had in flight and freed its tensor
+ * memory, so the device stays usable but that work's outputs are invalid.
  * Returns GDN_ERR_CUDA if synchronising or reading fails.
  */
 gdn_status_t gdn_get_device_status(void *stream, unsigned int *flags);

@@ -42,6 +42,17 @@ def test_every_declared_symbol_is_exported(lib):
     assert set(declared_functions()) == set(_lib.SIGNATURES)
 
 
+def test_wait_test_library_is_built_beside_it(lib):
+    """build() also makes libgdn_waittest.so (the abort-path test build) with
+    the same exports; nothing but its own test loads it."""
+    from gated_delta_rule_09_gb300 import build
+    assert os.path.exists(build.WAITTEST_LIB)
+    out = subprocess.run(["nm", "-D", "--defined-only", build.WAITTEST_LIB],
+                         capture_output=True, text=True, check=True).stdout
+    exported = set(l.split()[-1] for l in out.splitlines() if l.strip())
+    assert set(declared_functions()) <= exported
+
+
 def test_header_compiles_as_c():
     # The header is plain C: it must compile without CUDA headers.
     src = '#include "gdn.h"\nint main(void){ return (int)GDN_OK + (int)GDN_BF16; }\n'
