@@ -128,53 +128,60 @@ def _chunk(q, k, v, log_alpha, beta, eta, S0, o, S_final, C, cu_seqlens, stream,
 
 
 def gdn_chunk_fwd_scan(q, k, v, log_alpha, beta, S0=None, o=None, S_final=None, C=64,
-                       segments=0, workspace=None, stream=None):
+                       segments=0, workspace=None, stream=None, cu_seqlens=None):
     """``gdn_chunk_fwd`` with each sequence cut into ``segments`` pieces that
     run in parallel (0 = chosen by the library); returns ``(o, S_final)``.
-    ``workspace`` is a uint8 CUDA tensor of at least
-    ``gdn_chunk_fwd_scan_workspace_size(...)`` bytes, allocated here if None."""
-    B, T, H, dk, dv, _ = _check_args(q, k, v, log_alpha, beta, None, S0, o, S_final, None)
+    ``cu_seqlens`` (int32 CUDA tensor [N+1]) packs N sequences along the
+    token axis as in ``gdn_chunk_fwd``.  ``workspace`` is a uint8 CUDA tensor
+    of at least ``gdn_chunk_fwd_scan_workspace_size(...)`` bytes, allocated
+    here if None."""
+    B, T, H, dk, dv, N = _check_args(q, k, v, log_alpha, beta, None, S0, o, S_final, cu_seqlens)
     lib = _lib.load()
     if o is None:
         o = torch.empty((B, T, H, dv), dtype=q.dtype, device=q.device)
     if S_final is None:
-        S_final = torch.empty((B, H, dv, dk), dtype=torch.float32, device=q.device)
+        S_final = torch.empty((N, H, dv, dk), dtype=torch.float32, device=q.device)
     with torch.cuda.device(q.device):
-        need = gdn_chunk_fwd_scan_workspace_size(B, H, T, dk, dv, C, segments)
+        need = gdn_chunk_fwd_scan_workspace_size(N, H, T, dk, dv, C, segments,
+                                                 packed=cu_seqlens is not None)
         if workspace is None:
             workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
         _need_cuda("workspace", workspace, torch.uint8)
         st = lib.gdn_chunk_fwd_scan(
             _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(S0), _ptr(o),
-            _ptr(S_final), B, H, T, dk, dv, int(C), _DTYPES[q.dtype], int(segments),
-            _ptr(workspace), workspace.numel(), ctypes.c_void_p(_stream_handle(stream, q.device)))
-    _lib.check(st)
-    return o, S_final
-
-
-def gdn_chunk_fwd_scan_noalloc(q, k, v, log_alpha, beta, S0=None, o=None, S_final=None, C=64,
-                               segments=0, stream=None):
-    """``gdn_chunk_fwd_scan`` on the library's fixed device scratch (no
-    workspace, nothing allocated by the call; o and S_final must then be
-    passed in to allocate nothing at all).  Calls overlapping in time race."""
-    B, T, H, dk, dv, _ = _check_args(q, k, v, log_alpha, beta, None, S0, o, S_final, None)
-    lib = _lib.load()
-    if o is None:
-        o = torch.empty((B, T, H, dv), dtype=q.dtype, device=q.device)
-    if S_final is None:
-        S_final = torch.empty((B, H, dv, dk), dtype=torch.float32, device=q.device)
-    with torch.cuda.device(q.device):
-        st = lib.gdn_chunk_fwd_scan_noalloc(
-            _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(S0), _ptr(o),
-            _ptr(S_final), B, H, T, dk, dv, int(C), _DTYPES[q.dtype], int(segments),
+            _ptr(S_final), N, H, T, dk, dv, int(C), _ptr(cu_seqlens), _DTYPES[q.dtype],
+            int(segments), _ptr(workspace), workspace.numel(),
             ctypes.c_void_p(_stream_handle(stream, q.device)))
     _lib.check(st)
     return o, S_final
 
 
-def gdn_chunk_fwd_scan_workspace_size(B, H, T, d_k, d_v, C=64, segments=0):
-    """Bytes of device workspace gdn_chunk_fwd_scan needs (0: none)."""
-    return int(_lib.load().gdn_chunk_fwd_scan_workspace_size(B, H, T, d_k, d_v, int(C),
+def gdn_chunk_fwd_scan_noalloc(q, k, v, log_alpha, beta, S0=None, o=None, S_final=None, C=64,
+                               segments=0, stream=None, cu_seqlens=None):
+    """``gdn_chunk_fwd_scan`` on the library's fixed device scratch (no
+    workspace, nothing allocated by the call; o and S_final must then be
+    passed in to allocate nothing at all).  Calls overlapping in time race."""
+    B, T, H, dk, dv, N = _check_args(q, k, v, log_alpha, beta, None, S0, o, S_final, cu_seqlens)
+    lib = _lib.load()
+    if o is None:
+        o = torch.empty((B, T, H, dv), dtype=q.dtype, device=q.device)
+    if S_final is None:
+        S_final = torch.empty((N, H, dv, dk), dtype=torch.float32, device=q.device)
+    with torch.cuda.device(q.device):
+        st = lib.gdn_chunk_fwd_scan_noalloc(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(S0), _ptr(o),
+            _ptr(S_final), N, H, T, dk, dv, int(C), _ptr(cu_seqlens), _DTYPES[q.dtype],
+            int(segments), ctypes.c_void_p(_stream_handle(stream, q.device)))
+    _lib.check(st)
+    return o, S_final
+
+
+def gdn_chunk_fwd_scan_workspace_size(B, H, T, d_k, d_v, C=64, segments=0, packed=False):
+    """Bytes of device workspace gdn_chunk_fwd_scan needs (0: none); ``B`` is
+    the number of sequences and ``packed`` says whether they come packed
+    (cu_seqlens; ``T`` is then the packed length)."""
+    marker = ctypes.c_void_p(1) if packed else None  # only NULL-ness reaches the library
+    return int(_lib.load().gdn_chunk_fwd_scan_workspace_size(B, H, T, d_k, d_v, int(C), marker,
                                                               int(segments)))
 
 

@@ -30,12 +30,12 @@ SIGNATURES = {
                                      _i, _i, _i, _i, _i, _i, _vp, _i, _vp]),
     "gdn_chunk_fwd_eta": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                                          _i, _i, _i, _i, _i, _i, _vp, _i, _vp]),
-    "gdn_chunk_fwd_scan_workspace_size": (ctypes.c_size_t, [_i, _i, _i, _i, _i, _i, _i]),
+    "gdn_chunk_fwd_scan_workspace_size": (ctypes.c_size_t, [_i, _i, _i, _i, _i, _i, _vp, _i]),
     "gdn_chunk_fwd_scan": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
-                                          _i, _i, _i, _i, _i, _i, _i, _i, _vp, ctypes.c_size_t,
-                                          _vp]),
+                                          _i, _i, _i, _i, _i, _i, _vp, _i, _i, _vp,
+                                          ctypes.c_size_t, _vp]),
     "gdn_chunk_fwd_scan_noalloc": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
-                                                  _i, _i, _i, _i, _i, _i, _i, _i, _vp]),
+                                                  _i, _i, _i, _i, _i, _i, _vp, _i, _i, _vp]),
     "gdn_ut_inverse": (ctypes.c_int, [_vp, _vp, _i, _i, _i, _vp]),
     "gdn_decode_step": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                                        _i, _i, _i, _i, _i, _i, _vp]),

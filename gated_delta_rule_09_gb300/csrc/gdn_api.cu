@@ -142,6 +142,20 @@ int segment_count(int B, int H, int d_v, int nchunks, int segments)
     return (nchunks + per - 1) / per;
 }
 
+// Segments per sequence for a call: packed sequences (lengths on the device)
+// are cut into the same number of segments each, chosen from the average
+// length T / B when not given, and never more than the chunks of the whole
+// pack; a short sequence's trailing segments are then empty.
+int segment_count_for(int B, int H, int T, int d_v, int C, bool packed, int segments)
+{
+    if (!packed) return segment_count(B, H, d_v, (T + C - 1) / C, segments);
+    const long total_chunks = ((long)T + C - 1) / C;
+    const int avg = (int)((total_chunks + B - 1) / B);
+    int P = segments > 0 ? segments : choose_segments(B, H, d_v, avg > 0 ? avg : 1);
+    if (P > total_chunks) P = (int)total_chunks;
+    return P < 1 ? 1 : P;
+}
+
 gdn_status_t check_chunk(const void *q, const void *k, const void *v, const float *log_alpha,
                          const float *beta, const float *eta, const float *S0, void *o,
                          float *S_final, int B, int H, int T, int d_k, int d_v, int C,
@@ -297,11 +311,11 @@ gdn_status_t gdn_chunk_fwd_eta(const void *q, const void *k, const void *v,
 }
 
 size_t gdn_chunk_fwd_scan_workspace_size(int B, int H, int T, int d_k, int d_v, int C,
-                                         int segments)
+                                         const int32_t *cu_seqlens, int segments)
 {
     if (B <= 0 || H <= 0 || T <= 0 || d_k <= 0 || d_v <= 0 || (C != 16 && C != 32 && C != 64))
         return 0;
-    const int P = segment_count(B, H, d_v, (T + C - 1) / C, segments);
+    const int P = segment_count_for(B, H, T, d_v, C, cu_seqlens != nullptr, segments);
     return P <= 1 ? 0 : scan_layout(B, H, d_k, d_v, P).total;
 }
 
@@ -309,21 +323,20 @@ gdn_status_t gdn_chunk_fwd_scan(const void *q, const void *k, const void *v,
                                 const float *log_alpha, const float *beta,
                                 const float *S0, void *o, float *S_final,
                                 int B, int H, int T, int d_k, int d_v, int C,
-                                gdn_dtype_t dtype, int segments,
+                                const int32_t *cu_seqlens, gdn_dtype_t dtype, int segments,
                                 void *workspace, size_t workspace_bytes, void *stream)
 {
     GdnArgs a;
     bool nothing = false;
     gdn_status_t st = check_chunk(q, k, v, log_alpha, beta, nullptr, S0, o, S_final, B, H, T, d_k,
-                                  d_v, C, nullptr, dtype, &a, &nothing);
+                                  d_v, C, cu_seqlens, dtype, &a, &nothing);
     if (st != GDN_OK || nothing) return st;
     if (!gdn_tc_supported(a))
         return fail(GDN_ERR_UNSUPPORTED,
                     "the chunk-level scan runs on the tensor-core kernel: bf16, C = 64 and d_k, d_v "
                     "multiples of 8 (got dtype %d, d_k=%d, d_v=%d, C=%d)", (int)dtype, d_k, d_v, C);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const int nchunks = (T + C - 1) / C;
-    const int P = segment_count(B, H, d_v, nchunks, segments);
+    const int P = segment_count_for(B, H, T, d_v, C, cu_seqlens != nullptr, segments);
     int launches = 0, path = -1;
     if (P <= 1) {  // one segment per sequence: the plain forward pass
         st = launch_chunk(a, s, &launches, &path);
@@ -338,13 +351,14 @@ gdn_status_t gdn_chunk_fwd_scan(const void *q, const void *k, const void *v,
                     workspace ? workspace_bytes : (size_t)0);
     if (!aligned(workspace, 256))
         return fail(GDN_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
-    const size_t tokens = (size_t)B * T;
+    const size_t tokens = cu_seqlens ? (size_t)T : (size_t)B * T;
     const size_t nqk = tokens * H * d_k * 2, nv = tokens * H * d_v * 2;
     const size_t ng = tokens * H * sizeof(float), ns = (size_t)B * H * d_v * d_k * sizeof(float);
     if (overlaps(workspace, l.total, q, nqk) || overlaps(workspace, l.total, k, nqk) ||
         overlaps(workspace, l.total, v, nv) || overlaps(workspace, l.total, o, nv) ||
         overlaps(workspace, l.total, log_alpha, ng) || overlaps(workspace, l.total, beta, ng) ||
-        overlaps(workspace, l.total, S0, ns) || overlaps(workspace, l.total, S_final, ns))
+        overlaps(workspace, l.total, S0, ns) || overlaps(workspace, l.total, S_final, ns) ||
+        overlaps(workspace, l.total, cu_seqlens, cu_seqlens ? (size_t)(B + 1) * sizeof(int32_t) : 0))
         return fail(GDN_ERR_INVALID_ARG, "workspace overlaps an argument");
 
     uint8_t *ws = static_cast<uint8_t *>(workspace);
@@ -352,10 +366,8 @@ gdn_status_t gdn_chunk_fwd_scan(const void *q, const void *k, const void *v,
     float *Sin = reinterpret_cast<float *>(ws + l.sin);
     float *Bseg = reinterpret_cast<float *>(ws + l.bseg);
     float *Mseg = reinterpret_cast<float *>(ws + l.mseg);
-    const int per = (nchunks + P - 1) / P;  // chunks per segment
-
-    // (1) segment boundaries, as packed sequences over the B * T token rows
-    cudaError_t e = gdn_launch_segments(cu, B, P, T, per * C, s);
+    // (1) segment boundaries, as packed sequences over the token rows
+    cudaError_t e = gdn_launch_segments(cu, cu_seqlens, B, P, T, C, a.status, s);
     if (e != cudaSuccess) return fail(GDN_ERR_CUDA, "segment boundaries: %s", cudaGetErrorString(e));
     // (2) propagators: per segment, the state reached from zero and the transition
     GdnArgs pa = a;
@@ -400,10 +412,11 @@ gdn_status_t gdn_chunk_fwd_scan_noalloc(const void *q, const void *k, const void
                                         const float *log_alpha, const float *beta,
                                         const float *S0, void *o, float *S_final,
                                         int B, int H, int T, int d_k, int d_v, int C,
-                                        gdn_dtype_t dtype, int segments, void *stream)
+                                        const int32_t *cu_seqlens, gdn_dtype_t dtype, int segments,
+                                        void *stream)
 {
     t_msg[0] = '\0';
-    const size_t need = gdn_chunk_fwd_scan_workspace_size(B, H, T, d_k, d_v, C, segments);
+    const size_t need = gdn_chunk_fwd_scan_workspace_size(B, H, T, d_k, d_v, C, cu_seqlens, segments);
     if (need > kNoAllocScratchBytes)
         return fail(GDN_ERR_UNSUPPORTED,
                     "this problem needs %zu bytes of scan scratch; the fixed scratch holds %zu "
@@ -415,8 +428,8 @@ gdn_status_t gdn_chunk_fwd_scan_noalloc(const void *q, const void *k, const void
         if (st != GDN_OK) return st;
     }
     return gdn_chunk_fwd_scan(q, k, v, log_alpha, beta, S0, o, S_final, B, H, T, d_k, d_v, C,
-                              dtype, segments, scratch, need > 0 ? kNoAllocScratchBytes : 0,
-                              stream);
+                              cu_seqlens, dtype, segments, scratch,
+                              need > 0 ? kNoAllocScratchBytes : 0, stream);
 }
 
 gdn_status_t gdn_ut_inverse(const float *A, float *T, int count, int C, int method, void *stream)

@@ -50,7 +50,8 @@ cudaError_t gdn_launch_decode(const GdnDecodeArgs &a, cudaStream_t s, int *launc
 cudaError_t gdn_launch_scan(const float *S0, const float *Bseg, const float *Mseg, float *Sin,
                             int B, int P, int H, int dv, int dk, cudaStream_t s);
 // Segment boundaries of B equal-length sequences: cu[b * P + j] = b * T + min(j * seg, T).
-cudaError_t gdn_launch_segments(int32_t *cu, int B, int P, int T, int seg_tokens, cudaStream_t s);
+cudaError_t gdn_launch_segments(int32_t *cu, const int32_t *cu_seqlens, int B, int P, int T, int C,
+                                unsigned int *status, cudaStream_t s);
 
 // Batched UT inverse T = (I + StrictLower(A))^{-1}, C <= 64: method 0 blocked
 // forward substitution (CUDA cores, fp32), 1 doubling product (tcgen05).

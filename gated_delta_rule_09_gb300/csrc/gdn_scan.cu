@@ -92,18 +92,36 @@ __global__ void __launch_bounds__(kScanThreads) gdn_scan_kernel(
     }
 }
 
-__global__ void gdn_segments_kernel(int32_t *cu, int B, int P, int T, int seg_tokens)
+// Segment boundaries as packed sequences: sequence b (tokens [s_b, e_b), from
+// cu_seqlens when the input is packed, else [b T, (b + 1) T)) is cut into P
+// segments of ceil(chunks_b / P) chunks each; trailing segments of a short
+// sequence are empty.  Segment j of sequence b is unit b P + j, so the last
+// segment of b ends where b + 1 starts.  A span that is negative or runs past
+// T raises GDN_DEV_BAD_SEQLENS here and gets empty segments.
+__global__ void gdn_segments_kernel(int32_t *cu, const int32_t *cu_seqlens, int B, int P, int T,
+                                    int C, unsigned int *status)
 {
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
     const int n = B * P;
     if (i > n) return;
-    if (i == n) {
-        cu[i] = B * T;
-        return;
+    const int b = i / P, j = i % P;  // i == n: the end of the last sequence
+    long s, e;
+    if (cu_seqlens) {
+        s = cu_seqlens[i == n ? B : b];
+        e = i == n ? s : cu_seqlens[b + 1];
+    } else {
+        s = (long)(i == n ? B : b) * T;
+        e = i == n ? s : s + T;
     }
-    const int b = i / P, j = i % P;
-    const long start = (long)j * seg_tokens;
-    cu[i] = (int)((long)b * T + (start < T ? start : T));
+    const long total = cu_seqlens ? (long)T : (long)B * T;
+    if (s < 0 || e < s || e > total) {
+        if (j == 0 || i == n) atomicOr(status, 0x1u);
+        s = s < 0 ? 0 : (s > total ? total : s);
+        e = s;
+    }
+    const long nch = (e - s + C - 1) / C, per = (nch + P - 1) / P;
+    const long off = (long)j * per * C;
+    cu[i] = (int32_t)(s + (off < e - s ? off : e - s));
 }
 
 }  // namespace
@@ -120,9 +138,10 @@ cudaError_t gdn_launch_scan(const float *S0, const float *Bseg, const float *Mse
     return cudaGetLastError();
 }
 
-cudaError_t gdn_launch_segments(int32_t *cu, int B, int P, int T, int seg_tokens, cudaStream_t s)
+cudaError_t gdn_launch_segments(int32_t *cu, const int32_t *cu_seqlens, int B, int P, int T, int C,
+                                unsigned int *status, cudaStream_t s)
 {
     const int n = B * P + 1;
-    gdn_segments_kernel<<<(n + 255) / 256, 256, 0, s>>>(cu, B, P, T, seg_tokens);
+    gdn_segments_kernel<<<(n + 255) / 256, 256, 0, s>>>(cu, cu_seqlens, B, P, T, C, status);
     return cudaGetLastError();
 }

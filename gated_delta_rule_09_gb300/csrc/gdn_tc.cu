@@ -69,6 +69,7 @@ constexpr int kDVT = 128;    // d_v rows per unit (rows past d_v are zero paddin
 constexpr int kThreads = 384;  // producer: 3 pipelines x 4 warps; consumer: 3 x 4 warps
 constexpr int kNP = 3;         // producer pipelines (chunk c goes to pipeline c % 3)
 constexpr int kNOut = 5;       // outgoing buffers (chunk c uses buffer c % 5)
+constexpr int kOrderMax = 256;  // packed sequences ranked longest first up to this many
 #ifndef GDN_WAIT_TEST
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
 constexpr bool kWaitTest = false;
@@ -992,6 +993,39 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
     if (amax_over(amax)) atomicOr(a.status, 0x4u);
 }
 
+// Packed sequences of unequal length: grid slot z runs the sequence of rank z
+// by length, longest first (ties by index), so the longest chains start in
+// the first wave and the short ones fill in behind them, whatever order the
+// caller packed them in.  Every CTA ranks the (at most kOrderMax) lengths
+// itself, in shared memory that the ring reuses afterwards; a span that is
+// negative counts as empty here and is flagged where the unit reads it.
+__device__ __noinline__ int longest_first(const GdnArgs &a, uint8_t *sm, int tid)
+{
+    int *len = reinterpret_cast<int *>(sm);
+    int *pick = len + kOrderMax;
+#pragma unroll 1
+    for (int i = tid; i < a.N; i += kThreads) {
+        const int l = a.cu_seqlens[i + 1] - a.cu_seqlens[i];
+        len[i] = l > 0 ? l : 0;
+    }
+    __syncthreads();
+#pragma unroll 1
+    for (int i = tid; i < a.N; i += kThreads) {
+        const int li = len[i];
+        int r = 0;
+#pragma unroll 1
+        for (int j = 0; j < a.N; ++j) {
+            const int lj = len[j];
+            r += (lj > li) | ((lj == li) & (j < i));
+        }
+        if (r == (int)blockIdx.z) *pick = i;
+    }
+    __syncthreads();
+    const int n = *pick;
+    __syncthreads();  // the scratch is free again before anything reuses it
+    return n;
+}
+
 template <bool kProp>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 gdn_tc_kernel(const GdnArgs a, const __grid_constant__ CUtensorMap tm_q,
@@ -1002,7 +1036,9 @@ gdn_tc_kernel(const GdnArgs a, const __grid_constant__ CUtensorMap tm_q,
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const uint32_t rank = cluster_ctarank();  // 0 = producer, 1 = consumer
     const int tid = threadIdx.x, warp = tid >> 5;
-    const int vt = blockIdx.x >> 1, h = blockIdx.y, n = blockIdx.z;
+    const int vt = blockIdx.x >> 1, h = blockIdx.y;
+    const int n = a.cu_seqlens && a.N > 1 && a.N <= kOrderMax ? longest_first(a, sm, tid)
+                                                               : (int)blockIdx.z;
     const bool is_m = kProp && vt >= (a.dv + kDVT - 1) / kDVT;  // a propagator's identity rows
     const int v0 = is_m ? 0 : vt * kDVT;
 

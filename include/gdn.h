@@ -87,7 +87,9 @@ typedef enum { GDN_F32 = 0, GDN_BF16 = 1 } gdn_dtype_t;
  *              T is the packed length.  Chunks never cross a sequence; each
  *              sequence starts from its own S0[n].  Spans that are negative or
  *              run past T are skipped on the device and raise
- *              GDN_DEV_BAD_SEQLENS (see gdn_get_device_status).
+ *              GDN_DEV_BAD_SEQLENS (see gdn_get_device_status).  On the
+ *              tensor-core path, up to 256 packed sequences are started
+ *              longest first, whatever their order in the pack.
  *   dtype      GDN_F32 or GDN_BF16 (q, k, v and o share it).  fp32 runs in
  *              fp32 on CUDA cores.  bf16 runs on the tensor cores with fp16
  *              operands (11-bit significand) and fp32 accumulation and
@@ -152,12 +154,21 @@ gdn_status_t gdn_chunk_fwd_eta(const void *q, const void *k, const void *v,
  * gdn_chunk_fwd up to rounding; the work is about 2 + d_k / d_v times the
  * forward pass, spread over B * H * segments units instead of B * H.
  *
- * Arguments as gdn_chunk_fwd (no cu_seqlens: B sequences of T tokens), plus
- *   segments   pieces per sequence (1..ceil(T / C)); <= 0 lets the library
- *              choose from the device's SM count (1 means the plain pass)
+ * Arguments as gdn_chunk_fwd, packed sequences (cu_seqlens) included, plus
+ *   segments   pieces per sequence; <= 0 lets the library choose from the
+ *              device's SM count and the (average) sequence length (1 means
+ *              the plain pass).  Without cu_seqlens it is capped at
+ *              ceil(T / C) and no piece is empty.  With cu_seqlens every
+ *              sequence is cut into the same number of pieces of
+ *              ceil(chunks_n / segments) chunks, capped at the chunks of
+ *              the whole pack; a sequence shorter than that many chunks
+ *              leaves its last pieces empty.  A span that is negative or
+ *              runs past T raises GDN_DEV_BAD_SEQLENS; that sequence's
+ *              outputs are not written and its S_final is its S0.
  *   workspace  device scratch of at least
  *              gdn_chunk_fwd_scan_workspace_size(B, H, T, d_k, d_v, C,
- *              segments) bytes, 256-byte aligned, caller-owned, not
+ *              cu_seqlens, segments) bytes (only whether cu_seqlens is NULL
+ *              matters there), 256-byte aligned, caller-owned, not
  *              overlapping any argument; NULL is allowed when that size is 0
  *              or one segment is chosen.  Calls that share a workspace must
  *              not overlap in time.
@@ -167,13 +178,13 @@ gdn_status_t gdn_chunk_fwd_eta(const void *q, const void *k, const void *v,
  * device-to-device copy per sequence for S_final.
  */
 size_t gdn_chunk_fwd_scan_workspace_size(int B, int H, int T, int d_k, int d_v, int C,
-                                         int segments);
+                                         const int32_t *cu_seqlens, int segments);
 
 gdn_status_t gdn_chunk_fwd_scan(const void *q, const void *k, const void *v,
                                 const float *log_alpha, const float *beta,
                                 const float *S0, void *o, float *S_final,
                                 int B, int H, int T, int d_k, int d_v, int C,
-                                gdn_dtype_t dtype, int segments,
+                                const int32_t *cu_seqlens, gdn_dtype_t dtype, int segments,
                                 void *workspace, size_t workspace_bytes, void *stream);
 
 /*
@@ -195,7 +206,8 @@ gdn_status_t gdn_chunk_fwd_scan_noalloc(const void *q, const void *k, const void
                                         const float *log_alpha, const float *beta,
                                         const float *S0, void *o, float *S_final,
                                         int B, int H, int T, int d_k, int d_v, int C,
-                                        gdn_dtype_t dtype, int segments, void *stream);
+                                        const int32_t *cu_seqlens, gdn_dtype_t dtype,
+                                        int segments, void *stream);
 
 /*
  * gdn_decode_step — the same recurrence evaluated token by token, for decoding

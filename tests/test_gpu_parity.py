@@ -283,3 +283,40 @@ def test_zero_keys_pure_decay(gdn):
     x = I.custom(1, 2, 200, 128, 128, 64, dtype="bf16", seed=44, s0="normal_0.02")
     x["k"] = torch.zeros_like(x["k"])
     run_and_check(gdn, x, 64, "bf16")
+
+
+def repack(x, order):
+    """The packed inputs of ``x`` with its sequences in ``order``."""
+    cu = x["cu_seqlens"].tolist()
+    pieces = lambda t: torch.cat([t[:, cu[i]:cu[i + 1]] for i in order], dim=1).contiguous()
+    y = {kk: pieces(x[kk]) for kk in ("q", "k", "v", "log_alpha", "beta")}
+    lens = [cu[i + 1] - cu[i] for i in order]
+    y["cu_seqlens"] = torch.tensor(np.concatenate([[0], np.cumsum(lens)]), dtype=torch.int32)
+    y["S0"] = x["S0"][list(order)].contiguous()
+    return y
+
+
+@pytest.mark.parametrize("how", ["reversed", "shuffled", "longest_last"])
+def test_varlen_pack_order_is_bit_identical(gdn, how):
+    """The full-size varlen workload packed in another sequence order: every
+    sequence's outputs and final state are bit-identical to the given order's
+    (the units are independent whatever slot or SM they land on; the kernel
+    starts them longest first either way)."""
+    w = I.WORKLOADS["varlen_bf16"]
+    x = I.generate(w, seed=0)
+    N = len(x["lengths"])
+    order = {"reversed": list(range(N))[::-1],
+             "shuffled": list(np.random.default_rng(5).permutation(N)),
+             "longest_last": list(np.argsort(x["lengths"], kind="stable"))}[how]
+    y = repack(x, order)
+    dx, dy = _dev(x), _dev(y)
+    ox, Sx = gdn.gdn_chunk_fwd(dx["q"], dx["k"], dx["v"], dx["log_alpha"], dx["beta"], S0=dx["S0"],
+                               cu_seqlens=dx["cu_seqlens"])
+    oy, Sy = gdn.gdn_chunk_fwd(dy["q"], dy["k"], dy["v"], dy["log_alpha"], dy["beta"], S0=dy["S0"],
+                               cu_seqlens=dy["cu_seqlens"])
+    assert gdn.gdn_get_device_status() == 0
+    assert gdn.gdn_last_launch_count()[1] == 1
+    cx, cy = x["cu_seqlens"].tolist(), y["cu_seqlens"].tolist()
+    for j, i in enumerate(order):
+        assert torch.equal(ox[:, cx[i]:cx[i + 1]], oy[:, cy[j]:cy[j + 1]]), (how, i)
+        assert torch.equal(Sx[i], Sy[j]), (how, i)

@@ -53,7 +53,7 @@ def test_noalloc_rejects_oversize(gdn):
     buf = torch.zeros(16, dtype=torch.float32, device="cuda")
     p = ctypes.c_void_p(buf.data_ptr())
     lib = _lib.load()
-    st = lib.gdn_chunk_fwd_scan_noalloc(p, p, p, p, p, None, p, p, B, H, T, 128, 128, 64,
+    st = lib.gdn_chunk_fwd_scan_noalloc(p, p, p, p, p, None, p, p, B, H, T, 128, 128, 64, None,
                                         _lib.GDN_BF16, 64, None)
     assert st == _lib.GDN_ERR_UNSUPPORTED
     assert b"fixed scratch" in lib.gdn_get_last_error()
