@@ -630,7 +630,7 @@ def run_scan(args, world, rank, local):
 
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    B, H, T, dk, dv = 1, 8, 131072, 128, 128
+    B, H, T, dk, dv = 1, 8, args.scan_tokens, 128, 128
     x = I.custom(B, H, T, dk, dv, 64, dtype="bf16", seed=rank)
     keys = ("q", "k", "v", "log_alpha", "beta")
     d = {kk: x[kk].to(dev) for kk in keys}
@@ -681,7 +681,8 @@ def run_scan(args, world, rank, local):
     peaks, peak_src = load_peaks()
     gbs = byts / (ms * 1e-3) / 1e9
     line = {
-        "metric": SCAN_METRIC, "value": world * B * T / (ms_max * 1e-3), "unit": "tokens/s",
+        "metric": SCAN_METRIC.replace("T131072", "T%d" % T), "value": world * B * T / (ms_max * 1e-3),
+        "unit": "tokens/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
@@ -800,6 +801,8 @@ def main(argv=None):
                          "inverse by both methods")
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--scan-tokens", type=int, default=131072,
+                    help="--op scan: tokens of the one long sequence (smaller for profiling)")
     ap.add_argument("--ref-tokens", type=int, default=256,
                     help="tokens of each sequence per oracle step (all sequences, all heads)")
     ap.add_argument("--cpu-tokens", type=int, default=4096,

@@ -15,9 +15,14 @@
 //     x_0 = S0,   x_{s+1} = x_s M_s + B_s,
 //
 // and writes every x_s, the state each segment starts from.  Rows of the
-// state are independent: a warp owns two rows (four consecutive d_k elements
-// per lane), M_s is staged once per step in shared memory for the CTA's 16
-// rows, and x_s[i] is broadcast from the lane that holds it.
+// state are independent, so a CTA owns kRows rows of one (sequence, head) and
+// the grid has dv / kRows x H x B CTAs.  Per step, M_s (d_k x d_k) is staged
+// in shared memory, each of the 8 warps multiplies the CTA's rows by its
+// slice of d_k / 8 rows of M_s (a lane owns four columns, 16-byte accesses),
+// and the eight partial products are summed with B_s into the next x.  The
+// chain is short (one step per segment) and every step streams a whole M_s,
+// so the kernel is bound by that stream (L2 to the SMs); many small CTAs keep
+// every SM busy with it.
 #include <stdint.h>
 
 #include "gdn_internal.h"
@@ -25,70 +30,71 @@
 namespace {
 
 constexpr int kScanThreads = 256;
-constexpr int kRowsPerCta = 16;  // 8 warps x 2 rows
+constexpr int kScanWarps = kScanThreads / 32;
+constexpr int kRows = 4;  // state rows per CTA
 
 __global__ void __launch_bounds__(kScanThreads) gdn_scan_kernel(
     const float *__restrict__ S0, const float *__restrict__ Bseg, const float *__restrict__ Mseg,
     float *__restrict__ Sin, int P, int H, int dv, int dk)
 {
-    extern __shared__ float Ms[];  // [dk][dk]
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int h = blockIdx.y, b = blockIdx.z;
-    const int r0 = blockIdx.x * kRowsPerCta + 2 * warp;
+    extern __shared__ float smem[];
+    float *Ms = smem;                              // [dk][dk]
+    float *xT = Ms + dk * dk;                      // [dk][kRows]: the rows, transposed
+    float *part = xT + dk * kRows;                 // [warps][kRows][dk] partial products
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int h = blockIdx.y, b = blockIdx.z, r0 = blockIdx.x * kRows;
+    const int kslice = dk / kScanWarps;            // d_k is a multiple of 8
     const bool lane_ok = 4 * lane < dk;
-    bool row_ok[2];
-    float x[2][4];
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-        row_ok[r] = r0 + r < dv;
-        const float *src = S0 && row_ok[r] && lane_ok
-                               ? S0 + (((size_t)b * H + h) * dv + r0 + r) * dk + 4 * lane
-                               : nullptr;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) x[r][e] = src ? src[e] : 0.f;
+
+    for (int idx = tid; idx < kRows * dk; idx += kScanThreads) {
+        const int r = idx / dk, i = idx % dk;
+        xT[i * kRows + r] = S0 && r0 + r < dv ? S0[(((size_t)b * H + h) * dv + r0 + r) * dk + i] : 0.f;
     }
+    __syncthreads();
     for (int s = 0; s < P; ++s) {
         const size_t seg = (size_t)b * P + s;
-#pragma unroll
-        for (int r = 0; r < 2; ++r)
-            if (row_ok[r] && lane_ok) {
-                float *dst = Sin + ((seg * H + h) * dv + r0 + r) * dk + 4 * lane;
-                *reinterpret_cast<float4 *>(dst) = make_float4(x[r][0], x[r][1], x[r][2], x[r][3]);
-            }
-        if (s == P - 1) break;
-        __syncthreads();  // every warp is done with the previous M_s
-        const float4 *msrc = reinterpret_cast<const float4 *>(Mseg + (seg * H + h) * dk * dk);
-        for (int i = threadIdx.x; i < dk * dk / 4; i += kScanThreads)
-            reinterpret_cast<float4 *>(Ms)[i] = msrc[i];
-        float y[2][4];
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-            const float *bsrc = row_ok[r] && lane_ok
-                                    ? Bseg + ((seg * H + h) * dv + r0 + r) * dk + 4 * lane
-                                    : nullptr;
-#pragma unroll
-            for (int e = 0; e < 4; ++e) y[r][e] = bsrc ? bsrc[e] : 0.f;
+        const size_t row_base = (seg * H + h) * dv + r0;
+        for (int idx = tid; idx < kRows * dk; idx += kScanThreads) {
+            const int r = idx / dk, i = idx % dk;
+            if (r0 + r < dv) Sin[(row_base + r) * dk + i] = xT[i * kRows + r];
         }
+        if (s == P - 1) break;
+        const float4 *msrc = reinterpret_cast<const float4 *>(Mseg + (seg * H + h) * dk * dk);
+        for (int i = tid; i < dk * dk / 4; i += kScanThreads)
+            reinterpret_cast<float4 *>(Ms)[i] = msrc[i];
         __syncthreads();
-        for (int i4 = 0; i4 < dk / 4; ++i4) {
+        float acc[kRows][4];
 #pragma unroll
-            for (int e2 = 0; e2 < 4; ++e2) {
-                const int i = 4 * i4 + e2;
-                const float xa = __shfl_sync(0xffffffffu, x[0][e2], i4);
-                const float xb = __shfl_sync(0xffffffffu, x[1][e2], i4);
-                if (lane_ok) {
-                    const float4 m = *reinterpret_cast<const float4 *>(Ms + i * dk + 4 * lane);
-                    y[0][0] = fmaf(xa, m.x, y[0][0]); y[0][1] = fmaf(xa, m.y, y[0][1]);
-                    y[0][2] = fmaf(xa, m.z, y[0][2]); y[0][3] = fmaf(xa, m.w, y[0][3]);
-                    y[1][0] = fmaf(xb, m.x, y[1][0]); y[1][1] = fmaf(xb, m.y, y[1][1]);
-                    y[1][2] = fmaf(xb, m.z, y[1][2]); y[1][3] = fmaf(xb, m.w, y[1][3]);
+        for (int r = 0; r < kRows; ++r)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[r][e] = 0.f;
+        if (lane_ok) {
+            for (int i = warp * kslice; i < (warp + 1) * kslice; ++i) {
+                const float4 m = *reinterpret_cast<const float4 *>(Ms + i * dk + 4 * lane);
+                const float4 x = *reinterpret_cast<const float4 *>(xT + i * kRows);
+                const float xr[kRows] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                for (int r = 0; r < kRows; ++r) {
+                    acc[r][0] = fmaf(xr[r], m.x, acc[r][0]);
+                    acc[r][1] = fmaf(xr[r], m.y, acc[r][1]);
+                    acc[r][2] = fmaf(xr[r], m.z, acc[r][2]);
+                    acc[r][3] = fmaf(xr[r], m.w, acc[r][3]);
                 }
             }
+#pragma unroll
+            for (int r = 0; r < kRows; ++r)
+                *reinterpret_cast<float4 *>(part + (warp * kRows + r) * dk + 4 * lane) =
+                    make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
         }
+        __syncthreads();
+        for (int idx = tid; idx < kRows * dk; idx += kScanThreads) {
+            const int r = idx / dk, c = idx % dk;
+            float y = r0 + r < dv ? Bseg[(row_base + r) * dk + c] : 0.f;
 #pragma unroll
-        for (int r = 0; r < 2; ++r)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) x[r][e] = y[r][e];
+            for (int w = 0; w < kScanWarps; ++w) y += part[(w * kRows + r) * dk + c];
+            xT[c * kRows + r] = y;
+        }
+        __syncthreads();
     }
 }
 
@@ -129,11 +135,11 @@ __global__ void gdn_segments_kernel(int32_t *cu, const int32_t *cu_seqlens, int 
 cudaError_t gdn_launch_scan(const float *S0, const float *Bseg, const float *Mseg, float *Sin,
                             int B, int P, int H, int dv, int dk, cudaStream_t s)
 {
-    const size_t smem = (size_t)dk * dk * sizeof(float);
+    const size_t smem = ((size_t)dk * dk + (size_t)dk * kRows * (1 + kScanWarps)) * sizeof(float);
     cudaError_t e = cudaFuncSetAttribute(gdn_scan_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    dim3 grid((dv + kRowsPerCta - 1) / kRowsPerCta, H, B);
+    dim3 grid((dv + kRows - 1) / kRows, H, B);
     gdn_scan_kernel<<<grid, kScanThreads, smem, s>>>(S0, Bseg, Mseg, Sin, P, H, dv, dk);
     return cudaGetLastError();
 }
