@@ -382,7 +382,7 @@ gdn_status_t gdn_chunk_fwd_scan(const void *q, const void *k, const void *v,
     e = gdn_launch_tc(pa, s, &n);
     if (e != cudaSuccess) return fail(GDN_ERR_CUDA, "propagator pass: %s", cudaGetErrorString(e));
     // (3) the state each segment starts from
-    e = gdn_launch_scan(S0, Bseg, Mseg, Sin, B, P, H, d_v, d_k, s);
+    e = gdn_launch_scan(S0, Bseg, Mseg, Sin, B, P, H, d_v, d_k, a.status, s);
     if (e != cudaSuccess) return fail(GDN_ERR_CUDA, "segment scan: %s", cudaGetErrorString(e));
     // (4) the forward pass of every segment from its own start state
     GdnArgs fa = pa;

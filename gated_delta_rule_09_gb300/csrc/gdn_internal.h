@@ -48,8 +48,10 @@ cudaError_t gdn_launch_decode(const GdnDecodeArgs &a, cudaStream_t s, int *launc
 
 // Chunk-level scan over segments: x_{s+1} = x_s M_s + B_s (fp32, CUDA cores).
 cudaError_t gdn_launch_scan(const float *S0, const float *Bseg, const float *Mseg, float *Sin,
-                            int B, int P, int H, int dv, int dk, cudaStream_t s);
-// Segment boundaries of B equal-length sequences: cu[b * P + j] = b * T + min(j * seg, T).
+                            int B, int P, int H, int dv, int dk, unsigned int *status,
+                            cudaStream_t s);
+// Segment boundaries: sequence b (B sequences of T tokens, or packed through
+// cu_seqlens) cut into P segments of ceil(chunks_b / P) chunks each.
 cudaError_t gdn_launch_segments(int32_t *cu, const int32_t *cu_seqlens, int B, int P, int T, int C,
                                 unsigned int *status, cudaStream_t s);
 
