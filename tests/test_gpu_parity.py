@@ -320,3 +320,14 @@ def test_varlen_pack_order_is_bit_identical(gdn, how):
     for j, i in enumerate(order):
         assert torch.equal(ox[:, cx[i]:cx[i + 1]], oy[:, cy[j]:cy[j + 1]]), (how, i)
         assert torch.equal(Sx[i], Sy[j]), (how, i)
+
+
+@pytest.mark.parametrize("N", [256, 300])
+def test_many_packed_sequences(gdn, N):
+    """Many short packed sequences (ragged, some empty, some past a chunk):
+    up to 256 are ranked longest first inside the kernel, more run in the
+    given order; both against the oracle."""
+    lens = [int(x) for x in np.random.default_rng(N).integers(0, 90, size=N)]
+    x = I.custom(1, 1, 0, 64, 64, 64, dtype="bf16", seed=N, lengths=lens, s0="normal_0.02")
+    run_and_check(gdn, x, 64, "bf16")
+    assert gdn.gdn_last_launch_count()[1] == 1

@@ -172,3 +172,12 @@ def test_scan_packed_bad_span_is_flagged(gdn):
     eo = err(o[0, :n0].double().cpu().numpy(), ro[0, :n0], "bf16")
     es = err(S[0].double().cpu().numpy(), rS[0], "bf16", rounded=False)
     assert eo <= tol("bf16") and es <= tol("bf16"), (eo, es)
+
+
+def test_scan_packed_hybrid_head_shape(gdn):
+    """Packed sequences with d_k = 96, d_v = 192 through the scan: two value
+    tiles plus the identity tile per segment, 96-wide transitions."""
+    lens = [700, 130, 0, 1000]
+    x = I.custom(1, 2, 0, 96, 192, 64, dtype="bf16", seed=77, lengths=lens, s0="normal_0.02",
+                 beta="uniform_0_2")
+    check_packed(gdn, x, 5)
