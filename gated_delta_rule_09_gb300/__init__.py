@@ -262,13 +262,14 @@ def gdn_ut_inverse(A, T=None, method=0, stream=None):
 
 def gdn_get_device_status(stream=None):
     """Synchronise and return (then clear) the device status bits.  A timed-out
-    wait comes back as the GDN_DEV_WAIT_TIMEOUT bit (the C call's
-    GDN_ERR_TIMEOUT is that bit), not as an exception."""
+    wait or an fp16 overflow comes back as its bit (GDN_DEV_WAIT_TIMEOUT,
+    GDN_DEV_F16_RANGE; the C call's GDN_ERR_TIMEOUT / GDN_ERR_RANGE), not as
+    an exception."""
     handle = (torch.cuda.current_stream().cuda_stream if stream is None
               else getattr(stream, "cuda_stream", stream))
     flags = ctypes.c_uint(0)
     st = _lib.load().gdn_get_device_status(ctypes.c_void_p(handle), ctypes.byref(flags))
-    if st != _lib.GDN_ERR_TIMEOUT:
+    if st not in (_lib.GDN_ERR_TIMEOUT, _lib.GDN_ERR_RANGE):
         _lib.check(st)
     return flags.value
 

@@ -15,6 +15,7 @@ GDN_ERR_INVALID_ARG = 1
 GDN_ERR_UNSUPPORTED = 2
 GDN_ERR_CUDA = 3
 GDN_ERR_TIMEOUT = 4
+GDN_ERR_RANGE = 5
 GDN_F32 = 0
 GDN_BF16 = 1
 GDN_DEV_BAD_SEQLENS = 0x1

@@ -281,6 +281,8 @@ gdn_status_t gdn_get_device_status(void *stream, unsigned int *flags)
     *flags = v;
     if (v & GDN_DEV_WAIT_TIMEOUT)
         return fail(GDN_ERR_TIMEOUT, "a bounded device wait ran out (flags %#x): outputs invalid", v);
+    if (v & GDN_DEV_F16_RANGE)
+        return fail(GDN_ERR_RANGE, "a tensor-core operand left the fp16 range (flags %#x): outputs invalid", v);
     return GDN_OK;
 }
 

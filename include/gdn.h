@@ -43,9 +43,12 @@ typedef enum {
     GDN_ERR_INVALID_ARG = 1, /* null/misaligned pointer, bad size, overlap   */
     GDN_ERR_UNSUPPORTED = 2, /* shape or dtype outside the compiled set      */
     GDN_ERR_CUDA = 3,        /* a CUDA runtime call or a launch failed        */
-    GDN_ERR_TIMEOUT = 4      /* gdn_get_device_status: a bounded device wait
+    GDN_ERR_TIMEOUT = 4,     /* gdn_get_device_status: a bounded device wait
                                 ran out (GDN_DEV_WAIT_TIMEOUT is among the
                                 flags; the results of that call are invalid) */
+    GDN_ERR_RANGE = 5        /* gdn_get_device_status: a tensor-core operand
+                                left the fp16 range (GDN_DEV_F16_RANGE is
+                                among the flags; results are invalid) */
 } gdn_status_t;
 
 typedef enum { GDN_F32 = 0, GDN_BF16 = 1 } gdn_dtype_t;
@@ -279,6 +282,10 @@ gdn_status_t gdn_ut_inverse(const float *A, float *T, int count, int C, int meth
  * still written): a kernel gave up on a bounded wait, finished without
  * completing its work, drained what it had in flight and freed its tensor
  * memory, so the device stays usable but that work's outputs are invalid.
+ * Else GDN_ERR_RANGE when GDN_DEV_F16_RANGE is among them: an operand
+ * overflowed fp16, so the outputs it fed are wrong.  The other bits (a bad
+ * packed span: that sequence was skipped; fp16 precision: results are valid
+ * but carry fewer bits) come back with GDN_OK.
  * Returns GDN_ERR_CUDA if synchronising or reading fails.
  */
 gdn_status_t gdn_get_device_status(void *stream, unsigned int *flags);

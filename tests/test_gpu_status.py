@@ -31,11 +31,18 @@ def test_status_clean_for_ordinary_inputs(gdn):
 
 
 def test_f16_range_raised_by_large_values(gdn):
-    """v scaled by 1e6: representable in bf16, far past the fp16 maximum."""
+    """v scaled by 1e6: representable in bf16, far past the fp16 maximum.  The
+    C status read reports it as GDN_ERR_RANGE with the bit in its flags."""
+    import ctypes
     from gated_delta_rule_09_gb300 import _lib
     d = dev(I.custom(1, 2, 300, 128, 128, 64, dtype="bf16", seed=71))
     d["v"] = (d["v"].float() * 1e6).to(torch.bfloat16)
     assert run(gdn, d) == _lib.GDN_DEV_F16_RANGE
+    gdn.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"])
+    flags = ctypes.c_uint(0)
+    st = _lib.load().gdn_get_device_status(ctypes.c_void_p(torch.cuda.current_stream().cuda_stream),
+                                           ctypes.byref(flags))
+    assert st == _lib.GDN_ERR_RANGE and flags.value == _lib.GDN_DEV_F16_RANGE
 
 
 def test_f16_range_raised_by_large_initial_state(gdn):
