@@ -999,7 +999,9 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
 // caller packed them in.  Every CTA ranks the (at most kOrderMax) lengths
 // itself, in shared memory that the ring reuses afterwards; a span that is
 // negative counts as empty here and is flagged where the unit reads it.
-__device__ __noinline__ int longest_first(const GdnArgs &a, uint8_t *sm, int tid)
+// (Inlined with rolled loops: as a call, or unrolled, it cost the unpacked
+// path 1.6-3 % through the instruction layout.)
+__device__ __forceinline__ int longest_first(const GdnArgs &a, uint8_t *sm, int tid)
 {
     int *len = reinterpret_cast<int *>(sm);
     int *pick = len + kOrderMax;
