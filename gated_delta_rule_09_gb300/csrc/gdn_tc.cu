@@ -231,32 +231,19 @@ __device__ __forceinline__ uint32_t lane_addr(uint32_t tbase, int quad, uint32_t
     return tbase + (static_cast<uint32_t>(quad * 32) << 16) + col;
 }
 
-// Bounded waits, kept out of line (about twenty call sites), without calls of
-// their own.  Once this CTA has given up on one wait (GDN_DEV_WAIT_TIMEOUT),
+// The bounded wait, kept out of line (about twenty call sites) and without
+// calls of its own; one routine for every barrier, with acquire at cluster
+// scope (what the barriers the peer CTA arrives on need, and enough for the
+// others; one routine instead of two measured 3 % faster, by instruction
+// layout).  Once this CTA has given up on one wait (GDN_DEV_WAIT_TIMEOUT),
 // every wait that starts later is bounded by kDrainNs instead, so the kernel
 // winds down in milliseconds while the completions it still awaits come in:
 // every MMA batch, TMA load and shipment in flight is awaited by the walk that
 // follows it, and those finish in microseconds, so nothing asynchronous
 // outlives the CTA's tensor memory.  An aborted CTA issues no new TMA load or
 // shipment, and an aborted consumer releases no ring slot.
-__device__ __noinline__ bool wait_cta(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+__device__ __noinline__ bool wait_any(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
                                       unsigned int *status)
-{
-    const uint64_t lim = *abort_flag ? kDrainNs : kWaitLimitNs;
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer_ns();
-    for (;;) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if (globaltimer_ns() - t0 > lim) {
-            *abort_flag = 1;
-            atomicOr(status, 0x2u);
-            return false;
-        }
-    }
-}
-
-__device__ __noinline__ bool wait_cluster(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
-                                          unsigned int *status)
 {
     const uint64_t lim = *abort_flag ? kDrainNs : kWaitLimitNs;
     if (mbar_try_wait_cluster(bar, parity)) return true;
@@ -277,8 +264,7 @@ __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, bool cl
     // inline non-blocking probe first: most waits find their phase complete
     if (cluster_scope ? mbar_test_wait_cluster(bar, parity) : mbar_test_wait(bar, parity))
         return true;
-    return cluster_scope ? wait_cluster(bar, parity, abort_flag, status)
-                         : wait_cta(bar, parity, abort_flag, status);
+    return wait_any(bar, parity, abort_flag, status);
 }
 
 // ======================================================================
