@@ -319,6 +319,9 @@ __device__ __noinline__ void zero_rows(uint8_t *in, int nc, int t)
     fence_async_smem();
 }
 
+// kKS: K-steps of 16 over d_k in the MMAs whose contraction runs over d_k
+// (8 for d_k up to 128; 6 and 4 skip the zero padding of d_k <= 96, <= 64).
+template <int kKS>
 __device__ __forceinline__ void producer(const GdnArgs &a, const CUtensorMap *tm_q,
                                          const CUtensorMap *tm_k, uint8_t *sm, uint32_t tbase,
                                          long start, long len, int nchunks, int h)
@@ -394,7 +397,7 @@ __device__ __forceinline__ void producer(const GdnArgs &a, const CUtensorMap *tm
             const uint32_t id = idesc_bf16_f32(128, 64, 0, 0);
             const uint64_t dkq = sdesc_sw128(smem_u32(in), 16, 1024);
 #pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
+            for (int ks = 0; ks < kKS; ++ks) {
                 const uint32_t o = ((ks >> 2) * 16384 + (ks & 3) * 32) >> 4;
                 mma_f16kind(tcol, dkq + o, dkq + o, id, ks > 0);
             }
@@ -557,8 +560,9 @@ __device__ __noinline__ void store_partial(__nv_bfloat16 *o, uint32_t sq_addr, u
 }
 
 // kProp: propagator mode (a compile-time switch, so the plain pass carries
-// none of its branches).
-template <bool kProp>
+// none of its branches).  kKS: K-steps over d_k, as for the producer; the
+// state update's N (d_k columns of S) is 16 kKS.
+template <bool kProp, int kKS>
 __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm_q,
                                          const CUtensorMap *tm_k, const CUtensorMap *tm_v,
                                          uint8_t *sm, uint32_t tbase, long start, long len,
@@ -660,7 +664,7 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
             {
                 const float dC = __expf(gC);
                 #pragma unroll 1
-                for (int half = 0; half < 2; ++half) {  // one d_k half (64 columns) per step
+                for (int half = 0; half < (kKS + 3) / 4; ++half) {  // one d_k half (64 columns) per step
                     float x[32], y[32];
                     const uint32_t col = kColS + half * 64;
                     tmem_ld32(lane_addr(tbase, quad, col), x);
@@ -698,7 +702,7 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
                     const uint64_t dq = sdesc_sw128(smem_u32(slot) + kSlotKQ + 8192, 16, 1024);
                     const uint32_t csq = tbase + kColSQ + sl * 64;
 #pragma unroll
-                    for (int ks = 0; ks < 8; ++ks) {
+                    for (int ks = 0; ks < kKS; ++ks) {
                         const uint32_t o = ((ks >> 2) * 16384 + (ks & 3) * 32) >> 4;
                         mma_f16kind_ts(csq, tbase + kColS16 + ks * 8, dq + o, id_q, ks > 0);
                     }
@@ -714,7 +718,7 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
                 const uint32_t id_w = idesc_f16_f32(128, 64, 0, 1);
                 const uint64_t dw = sdesc_sw128(smem_u32(Wt), 8192, 1024);
 #pragma unroll
-                for (int ks = 0; ks < 8; ++ks)
+                for (int ks = 0; ks < kKS; ++ks)
                     mma_f16kind_ts(tbase + kColU, tbase + kColS16 + ks * 8, dw + ks * (2048 >> 4), id_w,
                                    !is_m || ks > 0);  // U = 0 in identity rows
                 mma_commit(&s->mma1);
@@ -755,7 +759,7 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
                 mbar_arrive(&s->epi1_done);  // U^T's columns are free for the next chunk
                 tc_fence_after();
                 const uint32_t ido = idesc_f16_f32(128, 64, 0, 0);
-                const uint32_t ids = idesc_f16_f32(128, 128, 0, 1);
+                const uint32_t ids = idesc_f16_f32(128, 16 * kKS, 0, 1);
                 const uint32_t sa = smem_u32(slot);
                 const uint64_t dvn = sdesc_sw128(smem_u32(VnT), 16, 1024);
                 const uint64_t dp = sdesc_sw128(sa + kOutP, 16, 1024);
@@ -1016,7 +1020,7 @@ __device__ __forceinline__ int longest_first(const GdnArgs &a, uint8_t *sm, int 
     return n;
 }
 
-template <bool kProp>
+template <bool kProp, int kKS>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 gdn_tc_kernel(const GdnArgs a, const __grid_constant__ CUtensorMap tm_q,
               const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v)
@@ -1102,8 +1106,8 @@ gdn_tc_kernel(const GdnArgs a, const __grid_constant__ CUtensorMap tm_q,
     tc_fence_after();
     const uint32_t tbase = *tmem_slot;
 
-    if (rank == 0) producer(a, &tm_q, &tm_k, sm, tbase, start, len, nchunks, h);
-    else consumer<kProp>(a, &tm_q, &tm_k, &tm_v, sm, tbase, start, len, nchunks, h, n, v0, is_m);
+    if (rank == 0) producer<kKS>(a, &tm_q, &tm_k, sm, tbase, start, len, nchunks, h);
+    else consumer<kProp, kKS>(a, &tm_q, &tm_k, &tm_v, sm, tbase, start, len, nchunks, h, n, v0, is_m);
 
     tc_fence_before();
     __syncthreads();
@@ -1163,7 +1167,11 @@ cudaError_t gdn_launch_tc(const GdnArgs &a, cudaStream_t s, int *launches)
         !make_map(&mv, a.v, tokens, a.H, a.dv))
         return cudaErrorInvalidValue;
     const bool prop = a.mode == 1;
-    auto kernel = prop ? gdn_tc_kernel<true> : gdn_tc_kernel<false>;
+    // K-steps over d_k: the plain pass skips d_k's zero padding; a propagator
+    // (rare, long sequences) keeps the full tile
+    auto kernel = prop ? gdn_tc_kernel<true, 8>
+                       : a.dk <= 64 ? gdn_tc_kernel<false, 4>
+                                    : a.dk <= 96 ? gdn_tc_kernel<false, 6> : gdn_tc_kernel<false, 8>;
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          kSmemBytes);
     if (e != cudaSuccess) return e;
