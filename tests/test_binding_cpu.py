@@ -75,3 +75,18 @@ def test_decode_rejects_bad_shapes(host_only, bad):
     a[bad] = wrong[bad]
     with pytest.raises(ValueError):
         gdn.gdn_decode_step(**a)
+
+
+@pytest.mark.parametrize("fn", [gdn.gdn_chunk_fwd_scan, gdn.gdn_chunk_fwd_scan_noalloc])
+def test_packed_scan_argument_checks(host_only, fn):
+    """The scan entry points take packed offsets with the rules of the plain
+    pass: B == 1, states per packed sequence."""
+    a, (B, T, H, dk, dv) = args(B=1)
+    cu = torch.tensor([0, 3, 8], dtype=torch.int32)
+    with pytest.raises(ValueError):  # S0 must be [N, H, d_v, d_k] with N = 2
+        fn(cu_seqlens=cu, S0=torch.zeros(1, H, dv, dk), **a)
+    b, _ = args(B=2)
+    with pytest.raises(ValueError):  # packed means B == 1
+        fn(cu_seqlens=torch.tensor([0, 8], dtype=torch.int32), **b)
+    with pytest.raises(RuntimeError, match="reached the library"):
+        fn(cu_seqlens=cu, S0=torch.zeros(2, H, dv, dk), **a)

@@ -136,3 +136,28 @@ def test_eta_entry_point_validation(lib):
     assert f(None) == 1 and lib.gdn_get_last_error()
     assert f(0x700002) == 1
     assert f(0x500010) == 1      # eta inside o
+
+
+def _scan_layout_bytes(nseg, H, dk, dv):
+    """The scan workspace as the header describes it: segment boundaries,
+    start states, segment final states and transitions, each 256-aligned."""
+    a = lambda x: (x + 255) // 256 * 256
+    return a((nseg + 1) * 4) + 2 * a(nseg * H * dv * dk * 4) + a(nseg * H * dk * dk * 4)
+
+
+@pytest.mark.parametrize("segments,expect_P", [(3, 3), (16, 16), (100, 16), (1, 1)])
+def test_scan_workspace_for_packed_sequences(lib, segments, expect_P):
+    """Packed sequences (a non-NULL cu_seqlens; only its NULL-ness is read
+    here) are cut into `segments` pieces each, capped at the chunks of the
+    whole pack (1000 tokens = 16 chunks of 64); one piece needs no workspace."""
+    B, H, T, dk, dv = 4, 2, 1000, 128, 128
+    size = lib.gdn_chunk_fwd_scan_workspace_size(B, H, T, dk, dv, 64, 0x1000, segments)
+    assert size == (0 if expect_P == 1 else _scan_layout_bytes(B * expect_P, H, dk, dv))
+
+
+def test_scan_workspace_unpacked_has_no_empty_segment(lib):
+    """Without cu_seqlens, B sequences of T tokens: 16 chunks asked for 5 pieces
+    become ceil(16 / ceil(16 / 5)) = 4 pieces of 4 chunks."""
+    B, H, T, dk, dv = 2, 2, 1024, 128, 128
+    size = lib.gdn_chunk_fwd_scan_workspace_size(B, H, T, dk, dv, 64, None, 5)
+    assert size == _scan_layout_bytes(B * 4, H, dk, dv)
