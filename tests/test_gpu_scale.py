@@ -93,3 +93,18 @@ def test_large_queries(gdn):
     x["q"] = bf16(x["q"].float() * 30.0)
     status, eo, es = check(gdn, x)
     assert status == 0
+
+
+def test_growing_gate_overflow_is_flagged(gdn):
+    """log alpha > 0 is allowed.  One chunk whose last four tokens grow the
+    gate by e^4 each, with q = k = 0 and beta = 0 there (so P, A and T'' stay
+    in range): the state-update operand V_new e^{g_C - g} is ~e^16 times V_new
+    and leaves fp16, while the exact final state (~5e6) is finite in fp32.
+    The kernel cannot represent it and must say so."""
+    from gated_delta_rule_09_gb300 import _lib
+    x = I.custom(1, 1, 64, 128, 128, 64, dtype="bf16", seed=7)
+    x["q"][:, 60:] = 0
+    x["k"][:, 60:] = 0
+    x["beta"][:, 60:] = 0
+    x["log_alpha"][:, 60:] = 4.0
+    check(gdn, x, expect_flag=_lib.GDN_DEV_F16_RANGE)
