@@ -108,3 +108,16 @@ def test_growing_gate_overflow_is_flagged(gdn):
     x["beta"][:, 60:] = 0
     x["log_alpha"][:, 60:] = 4.0
     check(gdn, x, expect_flag=_lib.GDN_DEV_F16_RANGE)
+
+
+@pytest.mark.parametrize("lo,hi", [(0.0, 0.02), (-0.05, 0.03)])
+def test_growing_gate_in_range(gdn, lo, hi):
+    """log alpha ~ U(lo, hi) with lo >= 0 (the state grows ~e^0.64 a chunk)
+    or of mixed sign: every decay factor the kernel splits or ships can then
+    exceed 1.  Five chunks stay well inside fp16, so the result must be
+    within the bound with a clean status."""
+    x = I.custom(1, 2, 320, 128, 128, 64, dtype="bf16", seed=85, s0="normal_0.02")
+    rng = np.random.default_rng(86)
+    x["log_alpha"] = torch.from_numpy(rng.uniform(lo, hi, tuple(x["log_alpha"].shape))).to(torch.float32)
+    status, eo, es = check(gdn, x)
+    assert status == 0 and eo <= TOL_BF16 and es <= TOL_BF16, (status, eo, es)
