@@ -664,31 +664,24 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
             {
                 const float dC = __expf(gC);
                 #pragma unroll 1
-                for (int half = 0; half < (kKS + 3) / 4; ++half) {  // one d_k half (64 columns) per step
-                    float x[32], y[32];
-                    const uint32_t col = kColS + half * 64;
+                // 32 d_k columns per step (in 64-column steps the larger loop body
+                // cost 2-3 % on the multi-wave workloads: instruction layout)
+                for (int qt = 0; qt < (kKS + 1) / 2; ++qt) {
+                    float x[32];
+                    const uint32_t col = kColS + qt * 32;
                     tmem_ld32(lane_addr(tbase, quad, col), x);
-                    tmem_ld32(lane_addr(tbase, quad, col + 32), y);
                     tmem_ld_wait();
-                    // fp16 copy: column 32 half + j of this row holds d_k elements
-                    // 64 half + 2j and 64 half + 2j + 1
-                    uint32_t pk[32];
+                    // fp16 copy: column 16 qt + j of this row holds d_k elements
+                    // 32 qt + 2j and 32 qt + 2j + 1
+                    uint32_t pk[16];
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        pk[j] = pack_f16(x[2 * j], x[2 * j + 1]);
-                        pk[16 + j] = pack_f16(y[2 * j], y[2 * j + 1]);
-                    }
+                    for (int j = 0; j < 16; ++j) pk[j] = pack_f16(x[2 * j], x[2 * j + 1]);
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) amax_fold(&amax, pk[j]);
-                    tmem_st32(lane_addr(tbase, quad, kColS16 + half * 32),
-                              *reinterpret_cast<const float(*)[32]>(pk));
+                    for (int j = 0; j < 16; ++j) amax_fold(&amax, pk[j]);
+                    tmem_st16(lane_addr(tbase, quad, kColS16 + qt * 16), pk);
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        x[j] *= dC;
-                        y[j] *= dC;
-                    }
+                    for (int j = 0; j < 32; ++j) x[j] *= dC;
                     tmem_st32(lane_addr(tbase, quad, col), x);
-                    tmem_st32(lane_addr(tbase, quad, col + 32), y);
                 }
                 tmem_st_wait();
             }
@@ -928,13 +921,13 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
         auto w_epilogue = [&](int c) {
             wait_bar(&s->w_mma, c & 1, false, abort_flag, a.status);
             tc_fence_after();
-            float x[32];
+            float x[16];
 #pragma unroll 1
-            for (int half = 0; half < 2; ++half) {
-                tmem_ld32(lane_addr(tbase, quad, kColSW + half * 32), x);
+            for (int qt = 0; qt < 4; ++qt) {  // 16 columns per step: a compact loop body
+                tmem_ld16(lane_addr(tbase, quad, kColSW + qt * 16), x);
                 tmem_ld_wait();
 #pragma unroll  // -W^T (from -T''): S (-W^T) accumulates onto U^T
-                for (int q = 0; q < 4; ++q) st_chunk(Wt, t, half * 4 + q, x + q * 8, &amax);
+                for (int q = 0; q < 2; ++q) st_chunk(Wt, t, qt * 2 + q, x + q * 8, &amax);
             }
             fence_async_smem();
             // the chain's first batch accumulates onto U^T: it is complete too
