@@ -270,6 +270,133 @@ __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, bool cl
 // ======================================================================
 // producer: the state-independent part of every chunk
 // ======================================================================
+// ---- T = (I + A)^{-1} with the two merges on warp-level tensor-core MMAs
+// (mma.sync m16n8k16, fp16 operands, fp32 accumulation): the products are
+// 16- and 32-wide, far too small for a tcgen05 round trip, and on CUDA cores
+// they are a serial stretch of the producer's per-chunk chain.  The operands
+// are rounded to fp16 as T' and T'' are afterwards, and pass the same range
+// check.
+// Fragment layouts are those of the PTX ISA for m16n8k16 (row.col): g = lane
+// / 4, q = lane % 4; A (16 x 16, row-major) rows g, g + 8 and columns
+// 2q, 2q + 1, 2q + 8, 2q + 9; B (16 x 8) rows 2q, 2q + 1, 2q + 8, 2q + 9 of
+// column g; D (16 x 8) rows g, g + 8 and columns 2q, 2q + 1.
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], const uint32_t (&b)[2])
+{
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+                 "{%8,%9}, {%0,%1,%2,%3};"
+                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                 : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
+// A fragment of the 16 x 16 block at (r0, c0) of an fp32 row-major matrix
+// (row stride ld, even), packed to fp16 and folded into the range check.
+__device__ __forceinline__ void frag_a(uint32_t (&a)[4], const float *M, int ld, int r0, int c0, int lane,
+                                       amax_t *amax)
+{
+    const int g = lane >> 2, q = lane & 3;
+    const float2 x0 = *reinterpret_cast<const float2 *>(M + (r0 + g) * ld + c0 + 2 * q);
+    const float2 x1 = *reinterpret_cast<const float2 *>(M + (r0 + g + 8) * ld + c0 + 2 * q);
+    const float2 x2 = *reinterpret_cast<const float2 *>(M + (r0 + g) * ld + c0 + 2 * q + 8);
+    const float2 x3 = *reinterpret_cast<const float2 *>(M + (r0 + g + 8) * ld + c0 + 2 * q + 8);
+    a[0] = pack_f16(x0.x, x0.y);
+    a[1] = pack_f16(x1.x, x1.y);
+    a[2] = pack_f16(x2.x, x2.y);
+    a[3] = pack_f16(x3.x, x3.y);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) amax_fold(amax, a[e]);
+}
+
+// B fragment of the 16 x 8 block at (k0, n0) of an fp32 row-major matrix.
+__device__ __forceinline__ void frag_b(uint32_t (&b)[2], const float *M, int ld, int k0, int n0, int lane,
+                                       amax_t *amax)
+{
+    const int g = lane >> 2, q = lane & 3;
+    const float *c = M + n0 + g;
+    b[0] = pack_f16(c[(k0 + 2 * q) * ld], c[(k0 + 2 * q + 1) * ld]);
+    b[1] = pack_f16(c[(k0 + 2 * q + 8) * ld], c[(k0 + 2 * q + 9) * ld]);
+    amax_fold(amax, b[0]);
+    amax_fold(amax, b[1]);
+}
+
+// D fragment (16 x 8 at (r0, n0)) times `sign` into an fp32 row-major matrix.
+__device__ __forceinline__ void store_d(const float (&d)[4], float *M, int ld, int r0, int n0, int lane,
+                                        float sign)
+{
+    const int g = lane >> 2, q = lane & 3;
+    *reinterpret_cast<float2 *>(M + (r0 + g) * ld + n0 + 2 * q) = make_float2(sign * d[0], sign * d[1]);
+    *reinterpret_cast<float2 *>(M + (r0 + g + 8) * ld + n0 + 2 * q) = make_float2(sign * d[2], sign * d[3]);
+}
+
+// In place over As as gdn_ut::ut_inverse_64 (the same blocks, the same
+// diagonal step); Xs is 32 x kLdX3 scratch.  128 threads, four warps.
+__device__ __forceinline__ void ut_inverse_64_mma(float *As, float *Xs, int t, uint32_t bar_id, amax_t *amax)
+{
+    float *Ts = As;
+    const int lane = t & 31, quad = t >> 5;
+    gdn_ut::ut_diag16(As, t);
+    named_sync(bar_id, 128);
+    // (2) 16 -> 32, T[1,0] = -T11 (A10 T00) for the block pairs (0,1), (2,3):
+    //     warps 0-1 the first pair, 2-3 the second, one 8-column half each.
+    {
+        const int pp = quad >> 1, n0 = 32 * pp + 8 * (quad & 1);
+        const int R = 16 * (2 * pp + 1), Cc = 32 * pp;
+        uint32_t a[4], b[2];
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
+        frag_a(a, As, kLdA, R, Cc, lane, amax);      // A10
+        frag_b(b, Ts, kLdA, Cc, n0, lane, amax);     // T00, this warp's columns
+        mma16816(d, a, b);
+        float *X = Xs + quad * 16 * 8;               // this warp's 16 x 8 product, stride 8
+        store_d(d, X, 8, 0, 0, lane, 1.f);
+        __syncwarp();
+        frag_a(a, Ts, kLdA, R, R, lane, amax);       // T11
+        frag_b(b, X, 8, 0, 0, lane, amax);
+        d[0] = d[1] = d[2] = d[3] = 0.f;
+        mma16816(d, a, b);
+        named_sync(bar_id, 128);                     // both halves have read A10
+        store_d(d, Ts, kLdA, R, n0, lane, -1.f);
+    }
+    named_sync(bar_id, 128);
+    // (3) 32 -> 64, T[32:64, 0:32] = -T2 (A21 T1): warp w the 16 x 16 quadrant
+    //     (rows 16 (w / 2), columns 16 (w % 2)) of each product.
+    {
+        const int r0 = 16 * (quad >> 1), c0 = 16 * (quad & 1);
+        float d[2][4];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) d[j][0] = d[j][1] = d[j][2] = d[j][3] = 0.f;
+#pragma unroll
+        for (int ks = 0; ks < 2; ++ks) {
+            uint32_t a[4];
+            frag_a(a, As, kLdA, 32 + r0, 16 * ks, lane, amax);  // A21
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                uint32_t b[2];
+                frag_b(b, Ts, kLdA, 16 * ks, c0 + 8 * j, lane, amax);  // T1
+                mma16816(d[j], a, b);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < 2; ++j) store_d(d[j], Xs, kLdX3, r0, c0 + 8 * j, lane, 1.f);
+        named_sync(bar_id, 128);
+#pragma unroll
+        for (int j = 0; j < 2; ++j) d[j][0] = d[j][1] = d[j][2] = d[j][3] = 0.f;
+        // T2 is lower triangular: rows 0-15 of it need only its columns 0-15
+        const int nks = r0 == 0 ? 1 : 2;
+        for (int ks = 0; ks < nks; ++ks) {
+            uint32_t a[4];
+            frag_a(a, Ts, kLdA, 32 + r0, 32 + 16 * ks, lane, amax);  // T2
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                uint32_t b[2];
+                frag_b(b, Xs, kLdX3, 16 * ks, c0 + 8 * j, lane, amax);
+                mma16816(d[j], a, b);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < 2; ++j) store_d(d[j], Ts, kLdA, 32 + r0, c0 + 8 * j, lane, -1.f);
+    }
+    named_sync(bar_id, 128);
+}
+
 // The A / P rows of a chunk whose total decay could push a split factor out
 // of fp32 range (every entry exponentiated on its own); rarely taken.  Inlined:
 // out of line it cost 3 % through the instruction layout of the hot loops
@@ -321,7 +448,9 @@ __device__ __noinline__ void zero_rows(uint8_t *in, int nc, int t)
 
 // kKS: K-steps of 16 over d_k in the MMAs whose contraction runs over d_k
 // (8 for d_k up to 128; 6 and 4 skip the zero padding of d_k <= 96, <= 64).
-template <int kKS>
+// kTcInv: the inverse's merges on warp-level tensor-core MMAs instead of
+// CUDA-core FMAs (chosen per launch, see gdn_launch_tc).
+template <int kKS, bool kTcInv>
 __device__ __forceinline__ void producer(const GdnArgs &a, const CUtensorMap *tm_q,
                                          const CUtensorMap *tm_k, uint8_t *sm, uint32_t tbase,
                                          long start, long len, int nchunks, int h)
@@ -486,7 +615,10 @@ __device__ __forceinline__ void producer(const GdnArgs &a, const CUtensorMap *tm
 
         // T = (I + A)^{-1}, blocked forward substitution in place
         if (k == 0 && t == 0) mbar_arrive(&s->gate[p]);
-        gdn_ut::ut_inverse_64(As, Xs, t, bar_id);
+        if constexpr (kTcInv)
+            ut_inverse_64_mma(As, Xs, t, bar_id, &amax);
+        else
+            gdn_ut::ut_inverse_64(As, Xs, t, bar_id);
         // -T'' = T diag(-beta e^g) and T' = T diag(eta), both shipped (T's upper
         // triangle is exactly zero, so the rows go out as they are)
         {
@@ -1013,7 +1145,7 @@ __device__ __forceinline__ int longest_first(const GdnArgs &a, uint8_t *sm, int 
     return n;
 }
 
-template <bool kProp, int kKS>
+template <bool kProp, int kKS, bool kTcInv>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 gdn_tc_kernel(const GdnArgs a, const __grid_constant__ CUtensorMap tm_q,
               const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v)
@@ -1099,7 +1231,7 @@ gdn_tc_kernel(const GdnArgs a, const __grid_constant__ CUtensorMap tm_q,
     tc_fence_after();
     const uint32_t tbase = *tmem_slot;
 
-    if (rank == 0) producer<kKS>(a, &tm_q, &tm_k, sm, tbase, start, len, nchunks, h);
+    if (rank == 0) producer<kKS, kTcInv>(a, &tm_q, &tm_k, sm, tbase, start, len, nchunks, h);
     else consumer<kProp, kKS>(a, &tm_q, &tm_k, &tm_v, sm, tbase, start, len, nchunks, h, n, v0, is_m);
 
     tc_fence_before();
@@ -1160,16 +1292,26 @@ cudaError_t gdn_launch_tc(const GdnArgs &a, cudaStream_t s, int *launches)
         !make_map(&mv, a.v, tokens, a.H, a.dv))
         return cudaErrorInvalidValue;
     const bool prop = a.mode == 1;
-    // K-steps over d_k: the plain pass skips d_k's zero padding; a propagator
-    // (rare, long sequences) keeps the full tile
-    auto kernel = prop ? gdn_tc_kernel<true, 8>
-                       : a.dk <= 64 ? gdn_tc_kernel<false, 4>
-                                    : a.dk <= 96 ? gdn_tc_kernel<false, 6> : gdn_tc_kernel<false, 8>;
-    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kSmemBytes);
-    if (e != cudaSuccess) return e;
     // a propagator adds one 128-row tile for the d_k identity rows
     dim3 grid(2 * ((a.dv + kDVT - 1) / kDVT + (prop ? 1 : 0)), a.H, a.N);
+    // The inverse's merges on tensor cores shorten the producer's chunk; that
+    // pays where the producer sets the pace, on grids of one wave of clusters
+    // (measured: B4 H16 T4096 d128 -2.0 %, B2 H4 T1024 d64 -4.3 %), and not on
+    // grids of several waves (+1.5 to +3 % on the packed, wide and
+    // d_k 96 / d_v 192 workloads), where the fp32 merges stay.
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    const bool one_wave = (long)grid.x / 2 * grid.y * grid.z <= sms / 2;
+    // K-steps over d_k: the plain pass skips d_k's zero padding; a propagator
+    // (rare, long sequences) keeps the full tile
+    auto kernel = prop ? gdn_tc_kernel<true, 8, false>
+                  : a.dk <= 64 ? (one_wave ? gdn_tc_kernel<false, 4, true> : gdn_tc_kernel<false, 4, false>)
+                  : a.dk <= 96 ? (one_wave ? gdn_tc_kernel<false, 6, true> : gdn_tc_kernel<false, 6, false>)
+                               : (one_wave ? gdn_tc_kernel<false, 8, true> : gdn_tc_kernel<false, 8, false>);
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
     kernel<<<grid, kThreads, kSmemBytes, s>>>(a, mq, mk, mv);
     *launches = 1;
     return cudaGetLastError();

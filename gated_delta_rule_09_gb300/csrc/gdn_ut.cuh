@@ -27,15 +27,14 @@ constexpr int kUtLd = 68;     // fp32 row stride of A / T: 16-byte rows, 4-bank 
 constexpr int kUtLdX2 = 20;   // row stride of the 16x16 merge scratch
 constexpr int kUtLdX3 = 36;   // row stride of the 32x32 merge scratch
 
-__device__ __forceinline__ void ut_inverse_64(float *As, float *Xs, int t, uint32_t bar_id)
+// (1) the four 16 x 16 diagonal blocks, in place, on warps 0-1: lane l of
+// warp w owns column l & 15 of block 2w + (l >> 4) and substitutes forward
+// down the rows (warps 2-3 pass through; the caller synchronises after it).
+__device__ __forceinline__ void ut_diag16(float *As, int t)
 {
-    using namespace sm100;
     float *Ts = As;
     const int lane = t & 31, quad = t >> 5;
-    constexpr int kLdA = kUtLd, kLdX2 = kUtLdX2, kLdX3 = kUtLdX3;
-    // (1) 16x16 diagonal blocks on warps 0-1: lane l of warp w owns column
-    //     l & 15 of block 2w + (l >> 4) and substitutes forward down the rows
-    //     (warps 2-3 wait at the barrier).
+    constexpr int kLdA = kUtLd;
     if (quad < 2) {
         const int b = 2 * quad + (lane >> 4), l = lane & 15;
         float tv[16];
@@ -53,6 +52,15 @@ __device__ __forceinline__ void ut_inverse_64(float *As, float *Xs, int t, uint3
 #pragma unroll
         for (int r = 0; r < 16; ++r) Ts[(16 * b + r) * kLdA + 16 * b + l] = tv[r];
     }
+}
+
+__device__ __forceinline__ void ut_inverse_64(float *As, float *Xs, int t, uint32_t bar_id)
+{
+    using namespace sm100;
+    float *Ts = As;
+    const int quad = t >> 5;
+    constexpr int kLdA = kUtLd, kLdX2 = kUtLdX2, kLdX3 = kUtLdX3;
+    ut_diag16(As, t);
     named_sync(bar_id, 128);
     // (2) 16 -> 32: T[1,0] = -T11 (A10 T00) for the block pairs (0,1), (2,3).
     //     64 threads per pair, each a 1x4 block of the 16x16 result with
