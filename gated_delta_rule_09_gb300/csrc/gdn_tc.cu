@@ -854,24 +854,24 @@ __device__ __forceinline__ void consumer(const GdnArgs &a, const CUtensorMap *tm
             // V_new^T -> VnT; V_new^T * e^{g_C - g} -> slot V region
             {
                 const float *ekc = gs + 2 * kC;
-                float u[32];
+                float u[16];
                 #pragma unroll 1
-                for (int half = 0; half < 2; ++half) {
-                    tmem_ld32(lane_addr(tbase, quad, kColU + half * 32), u);
-                    float e[32];
+                for (int qt = 0; qt < 4; ++qt) {  // 16 columns per step: a compact loop body
+                    tmem_ld16(lane_addr(tbase, quad, kColU + qt * 16), u);
+                    float e[16];
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) {
-                        const float4 f = *reinterpret_cast<const float4 *>(ekc + half * 32 + 4 * q);
+                    for (int q = 0; q < 4; ++q) {
+                        const float4 f = *reinterpret_cast<const float4 *>(ekc + qt * 16 + 4 * q);
                         e[4 * q] = f.x; e[4 * q + 1] = f.y; e[4 * q + 2] = f.z; e[4 * q + 3] = f.w;
                     }
                     tmem_ld_wait();
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) st_chunk(VnT, t, half * 4 + q, u + q * 8, &amax);
+                    for (int q = 0; q < 2; ++q) st_chunk(VnT, t, qt * 2 + q, u + q * 8, &amax);
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) u[j] *= e[j];
+                    for (int j = 0; j < 16; ++j) u[j] *= e[j];
 #pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        st_chunk(slot + kSlotV, t, half * 4 + q, u + q * 8, &amax);
+                    for (int q = 0; q < 2; ++q)
+                        st_chunk(slot + kSlotV, t, qt * 2 + q, u + q * 8, &amax);
                 }
             }
             fence_async_smem();
