@@ -627,7 +627,7 @@ __device__ __forceinline__ void producer(const GdnArgs &a, const CUtensorMap *tm
             uint8_t *dst = first ? out + kOutTpp : out + kOutTp;
             const float *scale = first ? s->colb[p] : s->eta[p];
             float x[8];
-#pragma unroll 1
+#pragma unroll 2  // two 8-column groups per step (rolled: 0.6 % slower on one-wave grids)
             for (int q = 0; q < 8; ++q) {
                 const float4 t0 = *reinterpret_cast<const float4 *>(Ts + j * kLdA + q * 8);
                 const float4 t1 = *reinterpret_cast<const float4 *>(Ts + j * kLdA + q * 8 + 4);
