@@ -13,11 +13,8 @@
 // exactly the zero upper blocks the merges read, so the loops need no
 // triangular bounds; the second product of each merge still stops at the
 // last row a warp owns, since the lower-triangular left factor is exactly
-// zero beyond it (the sums are unchanged, bit for bit).  `Xs` is merge
-// scratch of 32 x kUtLdX3 floats.  128 threads (t = 0..127, four whole
-// warps) synchronise on named barrier `bar_id`.  The tcgen05 producer can
-// also take step (1) alone (ut_diag16) and run (2) and (3) as warp-level
-// tensor-core products of its own.
+// zero beyond it (the sums are unchanged, bit for bit).  `Xs` is merge scratch of 32 x kUtLdX3 floats.  128 threads (t =
+// 0..127, four whole warps) synchronise on named barrier `bar_id`.
 #pragma once
 
 #include <stdint.h>
